@@ -1,0 +1,373 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test names what it pins and where the fact comes from.  None of these
+needs a GPU.
+"""
+
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import nvfp4_oracle as O
+from synthetic import generators as G
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- decode tables
+
+def _e2m1_from_bits(c):
+    """E2M1 from its bit fields: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0."""
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    mag = Fraction(m, 2) if e == 0 else (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1)
+    return -mag if s else mag
+
+
+def test_e2m1_table_matches_bit_field_formula():
+    t = O.e2m1_table()
+    for c in range(16):
+        assert Fraction(t[c]) == _e2m1_from_bits(c)
+        assert np.signbit(t[c]) == bool(c & 8)
+
+
+def test_e4m3_table_matches_torch_float8_decoder():
+    # Library decoder (torch.float8_e4m3fn) over all 256 encodings, NaNs included.
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    t = O.e4m3_table()
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(t))
+    assert set(np.flatnonzero(nan)) == {0x7F, 0xFF}
+    assert np.array_equal(t[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(t[~nan]), np.signbit(ref[~nan]))
+
+
+def test_unpack_low_nibble_is_even_k():
+    packed = np.array([[0x21, 0xF8]], dtype=np.uint8)
+    assert O.unpack_codes(packed).tolist() == [[1, 2, 8, 15]]
+    assert np.array_equal(O.pack_codes(O.unpack_codes(packed)), packed)
+
+
+# ---------------------------------------------------------------- GEMM definition
+
+def _frac_dequant(packed, sf):
+    codes = O.unpack_codes(packed)
+    R, K = codes.shape
+    e4 = [Fraction(x) if not np.isnan(x) else None for x in
+          torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()]
+    return [[_e2m1_from_bits(int(codes[r, k])) * e4[int(sf[r, k // 16])] for k in range(K)]
+            for r in range(R)]
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(1, 1, 16, 0), (3, 5, 64, 1), (8, 8, 128, 2), (7, 2, 64, 3)])
+def test_gemm_equals_exact_rational_brute_force(M, N, K, seed):
+    A = G.packed_codes_uniform(M, K, seed, "A")
+    B = G.packed_codes_uniform(N, K, seed, "B")
+    SFA = G.scales_with_zero_and_subnormal(M, K, seed, "SFA", 0.1, 0.2)
+    SFB = G.scales_with_zero_and_subnormal(N, K, seed, "SFB", 0.1, 0.2)
+    alpha = G.alpha_uniform(seed)
+    ref, abs_sum = O.gemm(A, SFA, B, SFB, alpha)
+    a = _frac_dequant(A, SFA)
+    b = _frac_dequant(B, SFB)
+    for m in range(M):
+        for n in range(N):
+            s = sum(a[m][k] * b[n][k] for k in range(K))
+            sa = sum(abs(a[m][k] * b[n][k]) for k in range(K))
+            assert Fraction(ref[m, n]) == s * Fraction(alpha)
+            assert Fraction(abs_sum[m, n]) == sa
+
+
+def test_single_block_dot_is_exact_in_float32():
+    # One 16-element block: the code sum is a multiple of 1/4 with |.| <= 576 and
+    # sfa*sfb has <= 8 significant bits, so the product is exact in FP32.
+    g = np.random.default_rng(5)
+    for _ in range(200):
+        A = g.integers(0, 256, size=(1, 8), dtype=np.uint8)
+        B = g.integers(0, 256, size=(1, 8), dtype=np.uint8)
+        sa = g.integers(0, 0x7F, size=(1, 1), dtype=np.uint8)
+        sb = g.integers(0, 0x7F, size=(1, 1), dtype=np.uint8)
+        ref, _ = O.gemm(A, sa, B, sb, 1.0)
+        assert float(np.float32(ref[0, 0])) == ref[0, 0]
+
+
+def test_all_scales_one_is_integer_gemm_on_twice_the_codes():
+    # With every scale = 1.0 (E4M3 0x38) the GEMM is an integer GEMM on 2*codes, /4.
+    M, N, K = 16, 24, 512
+    A = G.packed_codes_uniform(M, K, 7, "A")
+    B = G.packed_codes_uniform(N, K, 7, "B")
+    ones_a = np.full((M, K // 16), 0x38, dtype=np.uint8)
+    ones_b = np.full((N, K // 16), 0x38, dtype=np.uint8)
+    ref, _ = O.gemm(A, ones_a, B, ones_b, 1.0)
+    two = np.array([int(2 * _e2m1_from_bits(c)) for c in range(16)], dtype=np.int64)
+    ia = two[O.unpack_codes(A)]
+    ib = two[O.unpack_codes(B)]
+    exact = ia @ ib.T
+    assert np.array_equal(ref * 4, exact.astype(np.float64))
+
+
+def test_float64_gemm_equals_int64_gemm_on_square_workload_distribution():
+    # Square workloads: scales in [2^-4, 2^4] -> |product| <= 2^33.2 units of 2^-20,
+    # so float64 accumulation is exact over K <= 2^15.
+    M, N, K = 64, 48, 2048
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=3, scales="zero_sub")
+    ref, _ = O.gemm(A, SFA, B, SFB, 1.0)
+    units = O.gemm_exact_units(A, SFA, B, SFB)
+    assert np.array_equal(ref, units.astype(np.float64) * 2.0 ** -20)
+
+
+def test_sampled_and_tile_references_agree_with_full():
+    M, N, K = 40, 56, 256
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=4)
+    ref, abs_sum = O.gemm(A, SFA, B, SFB, 1.75)
+    rows = np.array([0, 5, 39, 17])
+    cols = np.array([55, 0, 3, 31])
+    r2, a2 = O.gemm_at(A, SFA, B, SFB, 1.75, rows, cols)
+    assert np.array_equal(r2, ref[rows, cols])
+    assert np.array_equal(a2, abs_sum[rows, cols])
+    rt, at = O.gemm_tile(A, SFA, B, SFB, 1.75, 8, 24, 16, 40)
+    assert np.array_equal(rt, ref[8:24, 16:40])
+
+
+def test_tolerance_formula_scales_with_alpha():
+    ref = np.array([256.0, -256.0, 0.0])
+    abs_sum = np.array([1e6, 1e6, 1e6])
+    tol = O.tolerance(ref, abs_sum, -2.0)
+    assert np.allclose(tol, [1.0 + 2.0, 1.0 + 2.0, 2.0])
+
+
+# ---------------------------------------------------------------- bf16 helpers
+
+def test_bf16_rne_matches_torch():
+    g = np.random.default_rng(11)
+    x = g.standard_normal(1_000_000).astype(np.float32) * np.float32(1e3)
+    # all tie patterns on a handful of exponents
+    base = np.arange(0, 1 << 16, 97, dtype=np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties, np.array([0.0, -0.0, np.inf, -np.inf, 3.4e38], dtype=np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = O.f32_to_bf16_rne(x)
+    nan = np.isnan(x)        # NaN payloads are a convention; both must stay NaN
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(np.isnan(O.bf16_bits_to_f64(got[nan])))
+    assert np.array_equal(O.bf16_bits_to_f64(ref), torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).double().numpy(), equal_nan=True)
+
+
+# ---------------------------------------------------------------- scale layout
+
+def test_pack_scales_golden_offsets():
+    for rows, K, r, c, off in _golden_rows("pack_scales_offsets.txt"):
+        rows, K, r, c, off = int(rows), int(K), int(r), int(c), int(off)
+        sf = np.zeros((rows, K // 16), dtype=np.uint8)
+        sf[r, c] = 0xA5
+        packed = O.pack_scales(sf)
+        assert packed.size == O.packed_scales_bytes(rows, K)
+        assert np.flatnonzero(packed).tolist() == [off], (rows, K, r, c)
+
+
+@pytest.mark.parametrize("R,K", [(1, 64), (128, 64), (129, 320), (300, 1024), (256, 48)])
+def test_pack_scales_is_bijection_with_zero_padding(R, K):
+    C = K // 16
+    ids = np.arange(R * C, dtype=np.int64)
+    # Values 1..255 repeat, so check the permutation through two byte planes.
+    lo = ((ids % 255) + 1).astype(np.uint8).reshape(R, C)
+    hi = (((ids // 255) % 255) + 1).astype(np.uint8).reshape(R, C)
+    plo, phi = O.pack_scales(lo), O.pack_scales(hi)
+    assert plo.size == (-(-R // 128)) * 128 * (-(-K // 64)) * 4
+    nz = np.flatnonzero(plo)
+    assert nz.size == R * C and np.array_equal(np.flatnonzero(phi), nz)
+    got = (phi[nz].astype(np.int64) - 1) * 255 + (plo[nz].astype(np.int64) - 1)
+    assert np.array_equal(np.sort(got), ids)
+
+
+def test_footprints_match_the_page():
+    for S, mib in _golden_rows("footprints.txt"):
+        S = int(S)
+        codes = 2 * (S * S // 2)
+        scales = 2 * (S * (S // 16))
+        assert O.packed_scales_bytes(S, S) == S * (S // 16)
+        assert (codes + scales) / 2 ** 20 == float(mib)
+
+
+# ---------------------------------------------------------------- quantisation
+
+def test_e2m1_rounding_golden():
+    for v, code in _golden_rows("e2m1_rounding.txt"):
+        got = int(O.e2m1_encode_rne_sat(np.array([float(v)], dtype=np.float32))[0])
+        assert got == int(code, 16), v
+
+
+def test_e2m1_encode_is_nearest_value_brute_force():
+    g = np.random.default_rng(2)
+    v = (g.standard_normal(20000) * 3).astype(np.float32)
+    codes = O.e2m1_encode_rne_sat(v)
+    vals = np.array([float(_e2m1_from_bits(c)) for c in range(16)])
+    for x, c in zip(v.astype(np.float64), codes):
+        err = abs(vals[c] - min(max(x, -6.0), 6.0))
+        assert err <= np.min(np.abs(vals - min(max(x, -6.0), 6.0))) + 0.0
+
+
+def test_e4m3_encode_matches_torch_rne_below_saturation():
+    g = np.random.default_rng(3)
+    v = np.concatenate([
+        np.exp(g.uniform(np.log(1e-5), np.log(460.0), 200000)),
+        O.e4m3_table()[:0x7F],                                     # exact values
+        (O.e4m3_table()[:0x7E] + O.e4m3_table()[1:0x7F]) / 2,      # exact ties
+    ]).astype(np.float32)
+    v = v[v < 464.0]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode_rne_satfinite(v), ref)
+    assert O.e4m3_encode_rne_satfinite(np.array([464.0, 1e30], dtype=np.float32)).tolist() == [0x7E, 0x7E]
+
+
+def test_quantize_invariants():
+    R, K = 64, 512
+    x = G.bf16_normal(R, K, 0, "x")
+    # a zero block and an all-negative tiny block
+    x[0, :16] = 0
+    x[1, 16:32] = 0x8001  # -tiny subnormal bf16
+    g = O.global_scale(x)
+    codes, sf = O.quantize(x, g)
+    assert codes.shape == (R, K // 2) and sf.shape == (R, K // 16)
+    dq = O.dequantize(codes, sf) * g
+    xf = O.bf16_bits_to_f64(x)
+    # every decoded value is bounded by 6 * scale * g
+    sc = np.repeat(O.e4m3_table()[sf], 16, axis=1) * g
+    assert np.all(np.abs(dq) <= 6 * sc + 0.0)
+    assert np.all(O.unpack_codes(codes)[0, :16] == 0) and sf[0, 0] == 0
+    assert np.all(O.unpack_codes(codes)[1, 16:32] == 0)
+    assert not np.any(O.unpack_codes(codes) == 8)              # no -0 codes
+    # the block's absmax element maps to code +-6 unless the scale was rounded
+    # up (then it may map to the next lower magnitude 4)
+    blocks = np.abs(xf).reshape(R, K // 16, 16)
+    arg = blocks.argmax(axis=2)
+    cmag = (O.unpack_codes(codes).reshape(R, K // 16, 16) & 7)
+    top = np.take_along_axis(cmag, arg[:, :, None], 2)[:, :, 0]
+    nz = sf != 0
+    assert np.all((top[nz] == 7) | (top[nz] == 6))
+    assert np.mean(top[nz] == 7) > 0.4
+    # relative reconstruction error of an NVFP4 tensor from N(0,1) is ~10 %
+    rel = np.linalg.norm(dq - xf) / np.linalg.norm(xf)
+    assert 0.03 < rel < 0.2
+
+
+def test_global_scale_reading():
+    x = G.bf16_normal(4, 64, 0, "x")
+    amax = np.max(np.abs(O.bf16_bits_to_f32(x)))
+    assert O.global_scale(x) == float(np.float32(amax) / np.float32(2688.0))
+    assert O.global_scale(np.zeros((2, 32), dtype=np.uint16)) == 1.0
+
+
+# ---------------------------------------------------------------- W4A16
+
+def test_w4a16_prepared_size_golden():
+    for N, K, nbytes in _golden_rows("w4a16_prepared_size.txt"):
+        assert O.w4a16_prepared_bytes(int(N), int(K)) == int(nbytes)
+    W = G.packed_codes_uniform(128, 256, 0, "W")
+    SW = G.scales_uniform_normal(128, 256, 0, "SW")
+    assert O.w4a16_prepare(W, SW).size == 18432
+
+
+def test_scale_reencode_identity_every_finite_e4m3():
+    # bf16(0x7000 | b << 4) == scale * 2^119 for every positive finite E4M3 scale,
+    # subnormals included (TileLang PR #3290, Design, "Weight layout").
+    t = O.e4m3_table()
+    for byte in range(1, 0x7F):
+        b = O.scale_reencode(byte)
+        assert 0 <= b < 256
+        bits = np.array([0x7000 | (b << 4)], dtype=np.uint16)
+        assert O.bf16_bits_to_f64(bits)[0] == t[byte] * 2.0 ** 119, hex(byte)
+
+
+def _emulate_register_dequant(wprep, N, K):
+    """Decode a Wprep buffer the way the W4A16 kernel's registers do (bf16 bit
+    manipulation, then one bfloat16 multiply rounded to nearest even), and return
+    float64 [N, K] weights times 2^-7 undone."""
+    blocks = np.asarray(wprep, dtype=np.uint8).reshape(N // 16, K // 64, 576)
+    out = np.zeros((N, K), dtype=np.float64)
+    mask = 0x81C081C0
+    for nt in range(N // 16):
+        for kc in range(K // 64):
+            blk = blocks[nt, kc]
+            for lane in range(32):
+                g, t = divmod(lane, 4)
+                words = blk[16 * lane:16 * lane + 16].view("<u4")
+                sb = blk[512 + 8 * g:512 + 8 * g + 8]
+                for j in range(4):
+                    w = int(words[j])
+                    r0 = w & mask
+                    r1 = (w << 3) & mask
+                    r2 = (w << 6) & mask
+                    r3 = (((w >> 4) & 0x00C000C0) | ((w >> 5) & 0x01000100) | ((w << 1) & 0x80008000))
+                    regs = (r0, r1, r2, r3)
+                    srow = (int(sb[2 * j]), int(sb[2 * j + 1]))          # rows g, g+8
+                    # reg -> (row offset, k offset of the low half)
+                    where = ((0, 0), (8, 0), (0, 8), (8, 8))
+                    for reg, (dr, dk) in zip(regs, where):
+                        s_bits = 0x7000 | (srow[dr // 8] << 4)
+                        for half in range(2):
+                            wb = (reg >> (16 * half)) & 0xFFFF
+                            prod = O.bf16_bits_to_f32(np.array([wb], np.uint16))[0] * \
+                                O.bf16_bits_to_f32(np.array([s_bits], np.uint16))[0]
+                            # bf16 multiply: exact here, so rounding the f32 product is the bf16 result
+                            pb = O.f32_to_bf16_rne(np.array([prod], np.float32))
+                            out[16 * nt + g + dr, 64 * kc + 16 * j + 2 * t + dk + half] = \
+                                O.bf16_bits_to_f64(pb)[0] * 2.0 ** 7
+    return out
+
+
+def test_wprep_register_dequant_every_scale_and_code():
+    # Every finite E4M3 scale byte, both signs and zero, with every code.
+    # (TileLang PR #3290, Tests: bit-exact emulation of the register dequant.)
+    scales = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], dtype=np.uint8)
+    n_rows = 16 * (-(-scales.size // 16))
+    K = 64
+    SW = np.zeros((n_rows, K // 16), dtype=np.uint8)
+    SW[:scales.size, :] = scales[:, None]
+    SW[:scales.size, 1] = scales[::-1][:, None][:, 0]
+    codes = np.tile(np.arange(16, dtype=np.uint8), (n_rows, K // 16))
+    codes = np.roll(codes, 3, axis=1)
+    W = O.pack_codes(codes)
+    wprep = O.w4a16_prepare(W, SW)
+    got = _emulate_register_dequant(wprep, n_rows, K)
+    want = O.dequantize(W, SW)
+    assert np.array_equal(np.abs(got), np.abs(want))
+    nzw = want != 0
+    assert np.array_equal(np.sign(got[nzw]), np.sign(want[nzw]))
+
+
+def test_w4a16_linear_equals_exact_rational_brute_force():
+    M, N, K = 3, 16, 64
+    x = G.bf16_normal(M, K, 1, "x")
+    W = G.packed_codes_uniform(N, K, 1, "W")
+    SW = G.scales_with_zero_and_subnormal(N, K, 1, "SW", 0.1, 0.2)
+    ref, abs_sum = O.w4a16_linear(x, W, SW, 0.5)
+    xf = [[Fraction(float(v)) for v in row] for row in O.bf16_bits_to_f64(x)]
+    w = _frac_dequant(W, SW)
+    for m in range(M):
+        for n in range(N):
+            s = sum(xf[m][k] * w[n][k] for k in range(K))
+            # float64 rounding of the sum: relative error far below the tolerance
+            assert abs(Fraction(ref[m, n]) - s * Fraction(1, 2)) <= Fraction(1, 2 ** 40) * (1 + abs(s))
+            assert abs(Fraction(abs_sum[m, n]) - sum(abs(xf[m][k] * w[n][k]) for k in range(K))) \
+                <= Fraction(1, 2 ** 40) * (1 + abs(s))
+
+
+def test_w4a16_sampled_agrees_with_full():
+    x = G.bf16_normal(5, 128, 2, "x")
+    W = G.packed_codes_uniform(32, 128, 2, "W")
+    SW = G.scales_uniform_normal(32, 128, 2, "SW")
+    ref, abs_sum = O.w4a16_linear(x, W, SW, 2.0)
+    r, a = O.w4a16_linear_at(x, W, SW, 2.0, [0, 4, 2], [31, 0, 7])
+    assert np.allclose(r, ref[[0, 4, 2], [31, 0, 7]], rtol=1e-15, atol=0)
