@@ -1,0 +1,203 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 block-scaled library.
+ *
+ * The library computes the NVFP4 block-scaled GEMM
+ *
+ *     D[m,n] = bf16( alpha * sum_k (A[m,k] * SFA[m,k/16]) * (B[n,k] * SFB[n,k/16]) )
+ *
+ * with E2M1 element codes, one unsigned E4M3 scale per 16 consecutive K elements,
+ * an FP32 per-tensor alpha, FP32 accumulation and BF16 output, plus the producers
+ * of its operands (quantisation, scale-factor packing) and a decode-shaped W4A16
+ * variant (BF16 activations times NVFP4 weights dequantised in registers).
+ *
+ * Sources (cited by page title and section):
+ *   [P1] Colfax Research, "Optimizing an NVFP4 Blockscaled GEMM on RTX PRO 6000
+ *        Blackwell GPU (SM120)".
+ *   [P2] TileLang PR #3290, "[CUDA] Add an SM120 W4A16 NVFP4 GEMM example for
+ *        decode-sized batches".
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the library
+ *     allocates no device memory and keeps no per-call state on the device.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and never synchronises the host.  Calls on different streams may run
+ *     concurrently.
+ *   - Errors are returned as nvfp4_status; nothing aborts or throws.  Arguments are
+ *     checked on the host; device data (codes, scales) is NOT validated: a NaN
+ *     (0x7F/0xFF) or negative scale byte given to nvfp4_gemm gives undefined
+ *     output values (never a fault).
+ *   - All sizes are 64-bit and all device offsets are computed in 64 bits.
+ *   - The device must be compute capability 10.3 (GB300); otherwise every compute
+ *     entry point returns NVFP4_ERR_UNSUPPORTED_DEVICE.
+ *   - Packed E2M1 codes: two 4-bit codes per byte, the LOW nibble holds the even k.
+ *     Code bits: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa; values
+ *     +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+ *   - E4M3 scale byte: bit 7 sign (must be 0 for GEMM inputs), bits 6..3 exponent
+ *     (bias 7), bits 2..0 mantissa; subnormals m*2^-9 and zero are valid scales.
+ */
+#ifndef NVFP4_GB300_H_
+#define NVFP4_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* nvfp4_stream_t;
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = -1,       /* null pointer, non-positive size, bad scale value */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = -2, /* a size violates a documented divisibility rule */
+  NVFP4_ERR_MISALIGNED = -3,        /* a pointer violates a documented alignment rule */
+  NVFP4_ERR_UNSUPPORTED_DEVICE = -4,/* current device is not compute capability 10.3 */
+  NVFP4_ERR_CUDA = -5,              /* a CUDA runtime/driver call or a launch failed */
+  NVFP4_ERR_TIMEOUT = -6            /* a kernel gave up a bounded wait (see nvfp4_device_error) */
+} nvfp4_status;
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* nvfp4_status_string(int status);
+
+/* ABI version of this header: major * 10000 + minor * 100 + patch. */
+int nvfp4_version(void);
+
+/*
+ * nvfp4_quantize -- BF16 activations/weights -> NVFP4 codes + row-major E4M3 scales.
+ *
+ * The pages name the format ([P2] Design: "packed E2M1, E4M3/UE4M3 block scales,
+ * global or per-column scale") but print no quantiser; this is the two-level
+ * NVFP4 recipe, with every step in IEEE float32, round to nearest even, unfused:
+ *   s      = E4M3_satfinite( (amax_block / 6) / global_scale )
+ *   code_k = E2M1_satfinite( x_k / (dec(s) * global_scale) )
+ *   a block whose scale is 0 gets all-zero codes; no -0 code is produced.
+ * The caller chooses global_scale (the usual choice is amax(|x|) / (6 * 448)).
+ *
+ *   x_bf16       [rows x K] bf16, row-major, contiguous, 16-byte aligned.
+ *   rows, K      rows >= 1, K >= 16, K % 16 == 0.
+ *   global_scale finite and > 0.
+ *   codes        [rows x K/2] bytes out, 8-byte aligned.
+ *   sf_rowmajor  [rows x K/16] bytes out (one E4M3 per 16-element block).
+ * Bit-exact (same bytes) as the IEEE reading above on every input without NaN;
+ * NaN inputs give unspecified codes.
+ */
+nvfp4_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t K, float global_scale,
+                            uint8_t* codes, uint8_t* sf_rowmajor, nvfp4_stream_t stream);
+
+/*
+ * Size in bytes of the packed scale-factor buffer of a [rows x K] operand:
+ * ceil(rows/128)*128 * ceil(K/64)*4.  Returns 0 for rows < 1 or K < 16 or K % 16 != 0.
+ */
+size_t nvfp4_packed_scales_bytes(int64_t rows, int64_t K);
+
+/*
+ * nvfp4_pack_scales -- row-major scales -> the 128x4-atom layout the GEMM reads.
+ *
+ * [P1] Version 5: within a 512-byte atom covering 128 rows x 64 K elements, the
+ * scale of row m and micro-block b (0..3) sits at byte 16*(m%32) + 4*((m/32)%4) + b;
+ * atoms are ordered K-fastest inside a 128-row band.  Padding rows and padding
+ * micro-blocks are written as zero.
+ *
+ *   sf_rowmajor  [rows x K/16] bytes.
+ *   rows, K      rows >= 1, K >= 16, K % 16 == 0.
+ *   sf_packed    nvfp4_packed_scales_bytes(rows, K) bytes out, 16-byte aligned.
+ */
+nvfp4_status nvfp4_pack_scales(const uint8_t* sf_rowmajor, int64_t rows, int64_t K,
+                               uint8_t* sf_packed, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm -- D = bf16(alpha * sum_k (A*SFA)(B*SFB)), FP32 accumulation.
+ *
+ * [P1] Version 1 (the block-scaled GEMM, K-major operands, BF16 output) and
+ * Version 3 (alpha multiplies the FP32 accumulator before the conversion).
+ * Runs on the tcgen05 tensor cores (kind::mxf4nvf4, scale_vec::4X).
+ *
+ *   A      [M x K/2] packed codes, K-major (row m holds k = 0..K-1), 16-byte aligned.
+ *   SFA    nvfp4_packed_scales_bytes(M, K) bytes in the packed layout, 16-byte aligned.
+ *   B      [N x K/2] packed codes, K-major, 16-byte aligned.
+ *   SFB    nvfp4_packed_scales_bytes(N, K) bytes, packed layout, 16-byte aligned.
+ *   alpha  finite FP32.
+ *   D_bf16 [M x N] bf16 out, row-major, 16-byte aligned.
+ *   M, N, K  M >= 1, N >= 8 and N % 8 == 0, K >= 64 and K % 64 == 0.
+ * Accuracy: |D - exact| <= 2^-8 |exact| + 1e-6 |alpha| sum_k |a_k b_k| per element.
+ * Deterministic: repeated calls give bit-identical D.
+ */
+nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                        float alpha, void* D_bf16, int64_t M, int64_t N, int64_t K,
+                        nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm_config -- nvfp4_gemm with an explicit kernel configuration (for tests
+ * and tuning).  config 0 is the automatic choice of nvfp4_gemm; the other values
+ * are listed by nvfp4_gemm_config_name.  Returns NVFP4_ERR_INVALID_ARG for an
+ * unknown config.
+ */
+nvfp4_status nvfp4_gemm_config(const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
+                               const uint8_t* SFB, float alpha, void* D_bf16, int64_t M,
+                               int64_t N, int64_t K, int config, nvfp4_stream_t stream);
+
+/* Name of a GEMM kernel configuration, or NULL past the last one (config >= 1). */
+const char* nvfp4_gemm_config_name(int config);
+
+/* Configuration nvfp4_gemm picks for (M, N, K) on the current device (>= 1), or a negative status. */
+int nvfp4_gemm_choose_config(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Size in bytes of a prepared W4A16 weight: N*K/2 + N*K/16, the size of the
+ * checkpoint tensors ([P2] Design, "Weight layout").  0 for invalid N, K.
+ */
+size_t nvfp4_w4a16_prepared_bytes(int64_t N, int64_t K);
+
+/*
+ * nvfp4_w4a16_prepare -- re-lay out an NVFP4 weight once for nvfp4_w4a16_linear.
+ *
+ * [P2] Design, "Weight layout": codes are moved into the fragment order of the
+ * decode kernel, each E4M3 scale is re-encoded as a byte b with
+ * bf16(0x7000 | b<<4) == |scale| * 2^119 (exact for every finite E4M3, subnormals
+ * included), zero scales zero their codes and negative scales flip their codes'
+ * signs.  The byte order is this library's own (specified with the oracle).
+ *
+ *   W_codes        [N x K/2] packed codes, K-major.
+ *   W_sf_rowmajor  [N x K/16] E4M3 scale bytes, row-major (sign allowed; NaN bytes
+ *                  give unspecified weights).
+ *   N, K           N % 16 == 0, K % 64 == 0, both >= their modulus.
+ *   Wprep          nvfp4_w4a16_prepared_bytes(N, K) bytes out, 16-byte aligned.
+ */
+nvfp4_status nvfp4_w4a16_prepare(const uint8_t* W_codes, const uint8_t* W_sf_rowmajor, int64_t N,
+                                 int64_t K, void* Wprep, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_w4a16_linear -- y = bf16(alpha * x * dequant(W)^T), FP32 accumulation.
+ *
+ * [P2] Summary and Design: BF16 activations, NVFP4 weights dequantised in
+ * registers, deterministic split-K (here a fixed-order reduction inside a thread
+ * block cluster, so no workspace is needed), BF16 output.
+ *
+ *   x_bf16  [M x K] bf16 row-major, 16-byte aligned.
+ *   Wprep   output of nvfp4_w4a16_prepare for (N, K).
+ *   alpha   the weight's FP32 global scale.
+ *   y_bf16  [M x N] bf16 out, row-major, 16-byte aligned.
+ *   M, N, K M >= 1; N % 128 == 0; K % 256 == 0.
+ * Accuracy: |y - exact| <= 2^-8 |exact| + 1e-6 |alpha| sum_k |x_k w_k|.
+ * Deterministic: repeated calls give bit-identical y.
+ */
+nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alpha, void* y_bf16,
+                                int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_device_error -- synchronise `stream`, then read the device-side error word
+ * of the current device.  Kernels never trap: a kernel that gives up one of its
+ * bounded waits (a pipeline barrier that did not complete within its time limit)
+ * records NVFP4_ERR_TIMEOUT there and returns early.  Returns NVFP4_OK if the word
+ * is clear, the recorded status otherwise, NVFP4_ERR_CUDA if the synchronisation
+ * failed.  clear != 0 resets the word.
+ */
+nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H_ */

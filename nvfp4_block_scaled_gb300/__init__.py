@@ -1,0 +1,227 @@
+"""Python binding of the GB300 NVFP4 block-scaled library (include/nvfp4.h).
+
+Argument marshalling only: every computation runs in the CUDA kernels of
+``_build/libnvfp4_gb300.so``.  The functions take torch CUDA tensors (torch is
+used for device memory and streams), pass their data pointers and the current
+CUDA stream to the C ABI, and raise ``NVFP4Error`` on a non-OK status.  There is
+no CPU fallback: if the shared library has not been built, the first call raises.
+
+Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
+  quantize, packed_scales_bytes, pack_scales, gemm, gemm_config_name,
+  gemm_choose_config, w4a16_prepared_bytes, w4a16_prepare, w4a16_linear,
+  device_error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libnvfp4_gb300.so")
+
+#: Every symbol include/nvfp4.h declares.
+ABI_SYMBOLS = (
+    "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_packed_scales_bytes",
+    "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_config_name",
+    "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
+    "nvfp4_w4a16_linear", "nvfp4_device_error",
+)
+
+NVFP4_OK = 0
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, fn: str, status: int, name: str):
+        super().__init__(f"{fn} failed: {name} ({status})")
+        self.status = status
+        self.status_name = name
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load (once) and return the shared library; raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"NVFP4 CUDA library not found at {path}; build it with "
+            "`python -m nvfp4_block_scaled_gb300.build` (there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    c_i64, c_p, c_f, c_i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+    sig = {
+        "nvfp4_status_string": (ctypes.c_char_p, [c_i]),
+        "nvfp4_version": (c_i, []),
+        "nvfp4_quantize": (c_i, [c_p, c_i64, c_i64, c_f, c_p, c_p, c_p]),
+        "nvfp4_packed_scales_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
+        "nvfp4_pack_scales": (c_i, [c_p, c_i64, c_i64, c_p, c_p]),
+        "nvfp4_gemm": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
+        "nvfp4_gemm_config": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_i, c_p]),
+        "nvfp4_gemm_config_name": (ctypes.c_char_p, [c_i]),
+        "nvfp4_gemm_choose_config": (c_i, [c_i64, c_i64, c_i64]),
+        "nvfp4_w4a16_prepared_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
+        "nvfp4_w4a16_prepare": (c_i, [c_p, c_p, c_i64, c_i64, c_p, c_p]),
+        "nvfp4_w4a16_linear": (c_i, [c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
+        "nvfp4_device_error": (c_i, [c_p, c_i]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().nvfp4_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != NVFP4_OK:
+        raise NVFP4Error(fn, status, status_string(status))
+
+
+def _stream(stream=None) -> int:
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return int(t.data_ptr())
+
+
+def _cuda(t, name, dtype=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---------------------------------------------------------------- entry points
+
+def version() -> int:
+    return int(load_library().nvfp4_version())
+
+
+def packed_scales_bytes(rows: int, K: int) -> int:
+    return int(load_library().nvfp4_packed_scales_bytes(int(rows), int(K)))
+
+
+def w4a16_prepared_bytes(N: int, K: int) -> int:
+    return int(load_library().nvfp4_w4a16_prepared_bytes(int(N), int(K)))
+
+
+def quantize(x, global_scale: float, codes=None, sf=None, stream=None):
+    """bf16 [rows, K] -> (codes uint8 [rows, K/2], row-major scales uint8 [rows, K/16])."""
+    import torch
+
+    _cuda(x, "x", torch.bfloat16)
+    rows, K = x.shape
+    if codes is None:
+        codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty((rows, K // 16), dtype=torch.uint8, device=x.device)
+    _cuda(codes, "codes", torch.uint8)
+    _cuda(sf, "sf", torch.uint8)
+    _check("nvfp4_quantize", load_library().nvfp4_quantize(
+        _ptr(x), rows, K, float(global_scale), _ptr(codes), _ptr(sf), _stream(stream)))
+    return codes, sf
+
+
+def pack_scales(sf, K: int | None = None, out=None, stream=None):
+    """Row-major scales [rows, K/16] -> packed 128x4-atom buffer (uint8, flat)."""
+    import torch
+
+    _cuda(sf, "sf", torch.uint8)
+    rows, C = sf.shape
+    K = 16 * C if K is None else int(K)
+    n = packed_scales_bytes(rows, K)
+    if out is None:
+        out = torch.empty((n,), dtype=torch.uint8, device=sf.device)
+    _cuda(out, "out", torch.uint8)
+    if out.numel() < n:
+        raise ValueError(f"out holds {out.numel()} bytes, needs {n}")
+    _check("nvfp4_pack_scales", load_library().nvfp4_pack_scales(_ptr(sf), rows, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def gemm(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, out=None, config: int = 0, stream=None):
+    """D = bf16(alpha * (A*SFA)(B*SFB)^T); A [M, K/2], B [N, K/2] packed codes, SFA/SFB packed."""
+    import torch
+
+    for t, nm in ((A, "A"), (SFA, "SFA"), (B, "B"), (SFB, "SFB")):
+        _cuda(t, nm, torch.uint8)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _cuda(out, "out", torch.bfloat16)
+    lib = load_library()
+    _check("nvfp4_gemm", lib.nvfp4_gemm_config(
+        _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
+        int(config), _stream(stream)))
+    return out
+
+
+def gemm_config_name(config: int):
+    r = load_library().nvfp4_gemm_config_name(int(config))
+    return None if r is None else r.decode()
+
+
+def gemm_configs():
+    names, i = [], 1
+    while (n := gemm_config_name(i)) is not None:
+        names.append(n)
+        i += 1
+    return names
+
+
+def gemm_choose_config(M: int, N: int, K: int) -> int:
+    r = int(load_library().nvfp4_gemm_choose_config(int(M), int(N), int(K)))
+    if r < 0:
+        _check("nvfp4_gemm_choose_config", r)
+    return r
+
+
+def w4a16_prepare(W, SW, out=None, stream=None):
+    """NVFP4 weight (codes [N, K/2], row-major scales [N, K/16]) -> prepared bytes."""
+    import torch
+
+    _cuda(W, "W", torch.uint8)
+    _cuda(SW, "SW", torch.uint8)
+    N, half = W.shape
+    K = 2 * half
+    n = w4a16_prepared_bytes(N, K)
+    if out is None:
+        out = torch.empty((max(n, 1),), dtype=torch.uint8, device=W.device)
+    _cuda(out, "out", torch.uint8)
+    _check("nvfp4_w4a16_prepare", load_library().nvfp4_w4a16_prepare(
+        _ptr(W), _ptr(SW), N, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def w4a16_linear(x, Wprep, alpha: float, N: int, out=None, stream=None):
+    """y = bf16(alpha * x * dequant(W)^T); x bf16 [M, K]."""
+    import torch
+
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(Wprep, "Wprep", torch.uint8)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("nvfp4_w4a16_linear", load_library().nvfp4_w4a16_linear(
+        _ptr(x), _ptr(Wprep), float(alpha), _ptr(out), M, int(N), K, _stream(stream)))
+    return out
+
+
+def device_error(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return (optionally clear) the device-side error status."""
+    return int(load_library().nvfp4_device_error(_stream(stream), 1 if clear else 0))

@@ -1,0 +1,213 @@
+// api.cu -- the extern "C" entry points declared in include/nvfp4.h: argument
+// checks, device checks, tensor-map encoding and dispatch to the kernel launchers.
+
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+nvfp4_status current_device(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  std::call_once(g_dev_once[dev], [dev]() {
+    DeviceInfo d;
+    d.device = dev;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) d.num_sms = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess) d.cc_major = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess) d.cc_minor = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
+      d.max_smem_optin = static_cast<size_t>(v);
+    d.ok = d.cc_major == 10 && d.cc_minor == 3 && d.num_sms > 0;
+    g_devices[dev] = d;
+  });
+  *out = g_devices[dev];
+  if (out->num_sms <= 0) return NVFP4_ERR_CUDA;
+  return out->ok ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED_DEVICE;
+}
+
+nvfp4_status encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                               uint64_t row_pitch, uint32_t box_inner, uint32_t box_outer,
+                               CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return NVFP4_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_pitch};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+inline cudaStream_t as_stream(nvfp4_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(int status) {
+  switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE";
+    case NVFP4_ERR_MISALIGNED: return "NVFP4_ERR_MISALIGNED";
+    case NVFP4_ERR_UNSUPPORTED_DEVICE: return "NVFP4_ERR_UNSUPPORTED_DEVICE";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+    case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+    default: return "NVFP4_ERR_UNKNOWN";
+  }
+}
+
+int nvfp4_version(void) { return 10000; }
+
+nvfp4_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t K, float global_scale, uint8_t* codes,
+                            uint8_t* sf_rowmajor, nvfp4_stream_t stream) {
+  if (x_bf16 == nullptr || codes == nullptr || sf_rowmajor == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (rows < 1 || K < 16 || rows > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
+  if (!(global_scale > 0.0f) || !(global_scale <= 3.4028234663852886e38f)) return NVFP4_ERR_INVALID_ARG;
+  if (K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 8)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_quantize(x_bf16, rows, K, global_scale, codes, sf_rowmajor, as_stream(stream), dev);
+}
+
+size_t nvfp4_packed_scales_bytes(int64_t rows, int64_t K) {
+  if (rows < 1 || K < 16 || K % 16 != 0 || rows > kMaxDim || K > kMaxDim) return 0;
+  return static_cast<size_t>((rows + 127) / 128) * 128 * static_cast<size_t>((K + 63) / 64) * 4;
+}
+
+nvfp4_status nvfp4_pack_scales(const uint8_t* sf_rowmajor, int64_t rows, int64_t K, uint8_t* sf_packed,
+                               nvfp4_stream_t stream) {
+  if (sf_rowmajor == nullptr || sf_packed == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (rows < 1 || K < 16 || rows > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
+  if (K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(sf_packed, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_pack_scales(sf_rowmajor, rows, K, sf_packed, as_stream(stream), dev);
+}
+
+static nvfp4_status gemm_checks(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                float alpha, void* D, int64_t M, int64_t N, int64_t K) {
+  if (A == nullptr || SFA == nullptr || B == nullptr || SFB == nullptr || D == nullptr)
+    return NVFP4_ERR_INVALID_ARG;
+  if (M < 1 || N < 8 || K < 64 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
+  if (!(alpha == alpha) || alpha > 3.4028234663852886e38f || alpha < -3.4028234663852886e38f)
+    return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(SFA, 16) || !aligned(SFB, 16) || !aligned(D, 16))
+    return NVFP4_ERR_MISALIGNED;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gemm_config(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                               float alpha, void* D_bf16, int64_t M, int64_t N, int64_t K, int config,
+                               nvfp4_stream_t stream) {
+  nvfp4_status st = gemm_checks(A, SFA, B, SFB, alpha, D_bf16, M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (config < 0 || config > gemm_num_configs()) return NVFP4_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  if (config == 0) config = gemm_choose_config(M, N, K, dev);
+  return launch_gemm(config, A, SFA, B, SFB, alpha, D_bf16, M, N, K, as_stream(stream), dev);
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
+                        void* D_bf16, int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream) {
+  return nvfp4_gemm_config(A, SFA, B, SFB, alpha, D_bf16, M, N, K, 0, stream);
+}
+
+const char* nvfp4_gemm_config_name(int config) { return gemm_config_name(config); }
+
+int nvfp4_gemm_choose_config(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 8 || K < 64) return NVFP4_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return gemm_choose_config(M, N, K, dev);
+}
+
+size_t nvfp4_w4a16_prepared_bytes(int64_t N, int64_t K) {
+  if (N < 16 || K < 64 || N % 16 != 0 || K % 64 != 0 || N > kMaxDim || K > kMaxDim) return 0;
+  return static_cast<size_t>(N) * static_cast<size_t>(K) / 2 + static_cast<size_t>(N) * static_cast<size_t>(K) / 16;
+}
+
+nvfp4_status nvfp4_w4a16_prepare(const uint8_t* W_codes, const uint8_t* W_sf_rowmajor, int64_t N, int64_t K,
+                                 void* Wprep, nvfp4_stream_t stream) {
+  if (W_codes == nullptr || W_sf_rowmajor == nullptr || Wprep == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (N < 16 || K < 64 || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
+  if (N % 16 != 0 || K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(Wprep, 16) || !aligned(W_codes, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_w4a16_prepare(W_codes, W_sf_rowmajor, N, K, Wprep, as_stream(stream), dev);
+}
+
+nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alpha, void* y_bf16, int64_t M,
+                                int64_t N, int64_t K, nvfp4_stream_t stream) {
+  if (x_bf16 == nullptr || Wprep == nullptr || y_bf16 == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (M < 1 || N < 128 || K < 256 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
+  if (!(alpha == alpha) || alpha > 3.4028234663852886e38f || alpha < -3.4028234663852886e38f)
+    return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x_bf16, 16) || !aligned(Wprep, 16) || !aligned(y_bf16, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_w4a16_linear(x_bf16, Wprep, alpha, y_bf16, M, N, K, as_stream(stream), dev);
+}
+
+nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const int a = read_device_error_gemm(clear != 0);
+  const int b = read_device_error_w4a16(clear != 0);
+  if (a == NVFP4_ERR_CUDA || b == NVFP4_ERR_CUDA) return NVFP4_ERR_CUDA;
+  if (a != 0) return static_cast<nvfp4_status>(a);
+  if (b != 0) return static_cast<nvfp4_status>(b);
+  return NVFP4_OK;
+}
+
+}  // extern "C"

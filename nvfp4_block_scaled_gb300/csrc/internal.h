@@ -1,0 +1,58 @@
+// internal.h -- host-side helpers shared by the translation units of the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  size_t max_smem_optin = 0;
+  bool ok = false;  // compute capability 10.3
+};
+
+// Cached properties of the current device (queried once per device).
+nvfp4_status current_device(DeviceInfo* out);
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+// 2-D UINT8 tensor map over a row-major byte matrix [outer x inner] with the given
+// row pitch, box [box_outer x box_inner], zero fill out of bounds.
+nvfp4_status encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                               uint64_t row_pitch, uint32_t box_inner, uint32_t box_outer,
+                               CUtensorMapSwizzle swizzle);
+
+// Per-translation-unit device error words (see ptx.cuh): returns the recorded
+// status (0 if none) or NVFP4_ERR_CUDA, optionally clearing it.
+int read_device_error_gemm(bool clear);
+int read_device_error_w4a16(bool clear);
+
+// Kernel launchers (defined next to their kernels).
+nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, uint8_t* codes,
+                             uint8_t* sf, cudaStream_t stream, const DeviceInfo& dev);
+nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out,
+                                cudaStream_t stream, const DeviceInfo& dev);
+
+int gemm_num_configs();
+const char* gemm_config_name(int config);
+int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
+                         const uint8_t* SFB, float alpha, void* D, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream, const DeviceInfo& dev);
+
+nvfp4_status launch_w4a16_prepare(const uint8_t* W, const uint8_t* SW, int64_t N, int64_t K, void* Wprep,
+                                  cudaStream_t stream, const DeviceInfo& dev);
+nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, void* y, int64_t M,
+                                 int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace nvfp4

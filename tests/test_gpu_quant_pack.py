@@ -1,0 +1,65 @@
+"""GPU parity of the operand producers: quantize and pack_scales are byte-exact
+against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_block_scaled_gb300 as nv
+from oracle import nvfp4_oracle as O
+from synthetic import generators as G
+from gpu_util import dev, dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("R,K", [(1, 64), (1, 16), (129, 320), (300, 1024), (256, 48), (8192, 5120)])
+def test_pack_scales_byte_exact(R, K):
+    sf = G.scales_with_zero_and_subnormal(R, K, 5, "sf", 0.05, 0.05)
+    got = nv.pack_scales(dev(sf), K).cpu().numpy()
+    want = O.pack_scales(sf)
+    assert got.shape == want.shape
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("R,K,std", [(64, 512, 1.0), (300, 5120, 1.0), (128, 5120, 0.02), (8192, 5120, 1.0)])
+def test_quantize_byte_exact(R, K, std):
+    x = G.bf16_normal(R, K, 7, "x", std)
+    g = O.global_scale(x)
+    codes, sf = nv.quantize(dev_bf16(x), g)
+    wc, ws = O.quantize(x, g)
+    assert np.array_equal(sf.cpu().numpy(), ws)
+    assert np.array_equal(codes.cpu().numpy(), wc)
+
+
+def test_quantize_rounding_ties_and_edge_values():
+    # Block 0: amax 6, g = 1 -> scale 1.0, so the elements hit every E2M1 tie exactly.
+    # Block 1: scale tie 1.0625 (between 1.0 and 1.125) -> even encoding 0x38.
+    # Block 2: scale tie 1.1875 (between 1.125 and 1.25) -> even encoding 0x3A.
+    # Block 3: all zero.  Block 4: tiny values whose scale underflows to 0.
+    # Block 5: values that saturate the scale (448) and the codes (6).
+    vals = np.zeros((1, 6 * 16), dtype=np.float32)
+    vals[0, 0:16] = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75,
+                     -2.5, -3.5, -5.0, 0.1]
+    vals[0, 16] = 6.375
+    vals[0, 17:32] = np.linspace(-6, 6, 15)
+    vals[0, 32] = 7.125
+    vals[0, 33:48] = np.linspace(-7, 7, 15)
+    vals[0, 64:80] = 1e-6
+    vals[0, 80:96] = 3e4
+    x = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    g = 1.0
+    codes, sf = nv.quantize(dev_bf16(x), g)
+    wc, ws = O.quantize(x, g)
+    assert ws[0, :3].tolist() == [0x38, 0x38, 0x3A]
+    assert ws[0, 3] == 0 and ws[0, 4] == 0 and ws[0, 5] == 0x7E
+    assert np.array_equal(sf.cpu().numpy(), ws)
+    assert np.array_equal(codes.cpu().numpy(), wc)
+
+
+def test_quantize_then_pack_feeds_gemm_layout():
+    x = G.bf16_normal(256, 512, 3, "x")
+    g = O.global_scale(x)
+    _, sf = nv.quantize(dev_bf16(x), g)
+    packed = nv.pack_scales(sf, 512).cpu().numpy()
+    assert np.array_equal(packed, O.pack_scales(O.quantize(x, g)[1]))
