@@ -57,14 +57,50 @@ nvfp4_status current_device(DeviceInfo* out) {
 nvfp4_status encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                                uint64_t row_pitch, uint32_t box_inner, uint32_t box_outer,
                                CUtensorMapSwizzle swizzle) {
+  return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner, outer, row_pitch, box_inner, box_outer,
+                        swizzle);
+}
+
+nvfp4_status encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                            uint64_t outer, uint64_t row_pitch, uint32_t box_inner, uint32_t box_outer,
+                            CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return NVFP4_ERR_CUDA;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_pitch};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status encode_tmap_u8_3d_chunks(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows,
+                                      uint32_t box_chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || K % 256 != 0) return NVFP4_ERR_CUDA;
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 256)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), 128};
+  const cuuint32_t box[3] = {128, box_rows, box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status encode_tmap_sf_3d(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_atoms,
+                               uint32_t box_bands) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || K % 64 != 0) return NVFP4_ERR_CUDA;
+  const int64_t bands = (rows + 127) / 128, atoms = K / 64;
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(atoms), static_cast<cuuint64_t>(bands)};
+  const cuuint64_t strides[2] = {512, static_cast<cuuint64_t>(atoms * 512)};
+  const cuuint32_t box[3] = {128, box_atoms, box_bands};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -267,6 +267,251 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// One pair of CTAs (a cluster of 2) computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64 per instruction).  Each CTA
+// stages its own 128 rows of A and its own 128 rows of B.
+//
+// Operand delivery is organised around the copy engine: on this GPU an SM's TMA
+// engine sustains far more bytes per cycle with large boxes (a 16 KB box moves
+// ~24 B/clk per SM under load, a 32 KB box ~60 B/clk).  So a pipeline stage
+// covers K = 512 and every copy is large: A and B arrive as one 32 KB 3-D box each
+// (two 128-byte-swizzled 16 KB sub-tiles, one per 256-wide K half), the stage's
+// scale atoms as one SFA box (8 atoms, 4 KB) and one SFB box (8 atoms of each of
+// the tile's two bands, 8 KB).  All of both CTAs' copies complete on the leader's
+// "full" barrier.  The leader's MMA thread moves the atoms into TMEM with
+// tcgen05.cp (in order with its MMAs), issues the stage's eight MMAs and releases
+// the stage to both CTAs with a multicast commit.  Eight epilogue warps per CTA
+// drain the accumulator (128 lanes x 256 columns) into a 128-byte-swizzled BF16
+// staging tile, release the accumulator, and write D with TMA stores.
+namespace pair {
+
+constexpr int kStages = 2;
+constexpr int kBKP = 512;                        // K per stage
+constexpr int kStepsP = kBKP / kMmaK;            // 8 MMAs per stage
+constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 2;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kABytes = 128 * (kBKP / 2);        // 32 KB: 2 sub-tiles of 128 rows x 128 B
+constexpr int kBBytes = 128 * (kBKP / 2);        // 32 KB
+constexpr int kSubTile = 128 * 128;              // 16 KB
+constexpr int kSFABytes = kStepsP * kAtom;       // 4 KB
+constexpr int kSFBBytes = 2 * kStepsP * kAtom;   // 8 KB: [band][atom]
+constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr int kOffSFA = kOffB + kStages * kBBytes;
+constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
+constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 4 boxes of 128 rows x 128 B (64 bf16 columns)
+constexpr int kOutBox = 128 * 128;
+constexpr int kOffBar = kOffOut + 4 * kOutBox;
+constexpr int kNumBars = 2 * kStages + 2;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kTmemCols = 512;
+constexpr int kSFACols = kStepsP * 4;   // MMA j reads SFA columns [4j, 4j + 4)
+constexpr int kSFBCols = kStepsP * 8;   // MMA j reads SFB columns [8j, 8j + 8) (band 0 then band 1)
+constexpr int kSFSlotCols = kSFACols + kSFBCols;
+constexpr int kTmemSF = 256;
+static_assert(kTmemSF + kStages * kSFSlotCols <= kTmemCols, "TMEM budget");
+
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(256 >> 3) << 17) |
+                            (static_cast<uint32_t>(256 >> 4) << 24);
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                          const __grid_constant__ CUtensorMap tmD, float alpha, int K, int tiles_m, int tiles_n,
+                          int group_n) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + kOffBar;             // both CTAs' copies (leader's copy is used)
+  const uint32_t bar_empty = bar_full + 8 * kStages;     // stage released by the MMAs (both CTAs)
+  const uint32_t bar_accf = bar_empty + 8 * kStages;
+  const uint32_t bar_acce = bar_accf + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair_id = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_accf, 1);
+    mbar_init(bar_acce, 2 * kEpiWarps);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmSFA);
+    prefetch_tensormap(&tmSFB);
+    prefetch_tensormap(&tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int num_tiles = tiles_m * tiles_n;
+  const int KB = (K + kBKP - 1) / kBKP;
+  const int KG = K / kMmaK;  // scale atoms per 128-row band
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t full_leader = map_to_rank(bar_full, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+        int mt, nt;
+        tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
+        const int a_row = mt * 256 + static_cast<int>(rank) * 128;
+        const int b_row = nt * 256 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
+          const uint32_t fb = full_leader + 8 * stage;
+          tma_load_3d_pair(sbase + kOffA + stage * kABytes, &tmA, fb, 0, a_row, 2 * kb);
+          tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, 2 * kb);
+          tma_load_3d_pair(sbase + kOffSFA + stage * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
+                           mt * 2 + static_cast<int>(rank));
+          tma_load_3d_pair(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, kb * kStepsP, nt * 2);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      // Drain: wait until every stage has been released once more, so that no commit
+      // arrival (and no copy of this CTA) is still in flight when the CTA exits.
+      for (int i = 0; i < kStages && !*abort_flag; ++i) {
+        if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) break;
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      if (*abort_flag && leader) {
+        for (int i = 0; i < kStages; ++i) mbar_wait_for(bar_full + 8 * i, 0, 10000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader CTA)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+        if (!mbar_wait(bar_acce, acc_phase ^ 1, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const int nk = min(kStepsP, KG - kb * kStepsP);
+          const uint32_t sfa_t = tmem + kTmemSF + stage * kSFSlotCols;
+          const uint32_t sfb_t = sfa_t + kSFACols;
+          const uint32_t sA = sbase + kOffA + stage * kABytes;
+          const uint32_t sB = sbase + kOffB + stage * kBBytes;
+          const uint32_t sSFA = sbase + kOffSFA + stage * kSFABytes;
+          const uint32_t sSFB = sbase + kOffSFB + stage * kSFBBytes;
+          for (int j = 0; j < nk; ++j) {
+            tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, make_sdesc(sSFB + j * kAtom, 0, 128, 0));
+            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, make_sdesc(sSFB + (kStepsP + j) * kAtom, 0, 128, 0));
+          }
+          for (int j = 0; j < nk; ++j) {
+            const uint32_t koff = (j >> 2) * kSubTile + (j & 3) * (kMmaK / 2);
+            const uint64_t adesc = make_sdesc(sA + koff, 16, 1024, 2);
+            const uint64_t bdesc = make_sdesc(sB + koff, 16, 1024, 2);
+            tc_mma_nvf4_pair(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(bar_accf, 0x3);
+        acc_phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (8 warps, both CTAs)
+    const int q = warp & 3;                        // TMEM lane quarter of this warp
+    const int h = (warp - kFirstEpiWarp) >> 2;     // column half (0: columns 0..127, 1: 128..255)
+    const uint32_t acce_leader = map_to_rank(bar_acce, 0);
+    const uint32_t out_base = sbase + kOffOut;
+    const int r = q * 32 + lane;                   // accumulator row = TMEM lane
+    uint32_t acc_phase = 0;
+    bool stored = false;
+    for (int t = pair_id; t < num_tiles; t += num_pairs) {
+      int mt, nt;
+      tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
+      if (!warp_wait(bar_accf, acc_phase, abort_flag)) break;
+      tc_fence_after();
+      if (stored) {  // the previous tile's stores must have finished reading the staging tile
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+      }
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        const int col0 = h * 128 + c32 * 32;
+        uint32_t v[32];
+        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
+        tc_wait_ld();
+        const uint32_t box = out_base + (2 * h + (c32 >> 1)) * kOutBox + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = (c32 & 1) * 4 + cc;   // 16-byte chunk (8 columns) within the 128-byte box row
+          uint32_t p0 = pack_bf16x2(alpha * __uint_as_float(v[8 * cc + 0]), alpha * __uint_as_float(v[8 * cc + 1]));
+          uint32_t p1 = pack_bf16x2(alpha * __uint_as_float(v[8 * cc + 2]), alpha * __uint_as_float(v[8 * cc + 3]));
+          uint32_t p2 = pack_bf16x2(alpha * __uint_as_float(v[8 * cc + 4]), alpha * __uint_as_float(v[8 * cc + 5]));
+          uint32_t p3 = pack_bf16x2(alpha * __uint_as_float(v[8 * cc + 6]), alpha * __uint_as_float(v[8 * cc + 7]));
+          const uint32_t addr = box + ((c ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(p0), "r"(p1), "r"(p2), "r"(p3)
+                       : "memory");
+        }
+      }
+      // Accumulator read out: hand it back to the MMA issuer.
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_cluster(acce_leader);
+        const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
+          tma_store_2d(&tmD, out_base + (2 * h + hb) * kOutBox + q * 32 * 128, nt * 256 + h * 128 + hb * 64, row0);
+        bulk_commit_group();
+      }
+      stored = true;
+      acc_phase ^= 1;
+    }
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+}  // namespace pair
+
 // ------------------------------------------------------------------ host side
 
 struct ConfigEntry {
@@ -277,6 +522,7 @@ struct ConfigEntry {
 constexpr ConfigEntry kConfigs[] = {
     {"1cta_128x256_s3_acc1", 256},
     {"1cta_128x128_s4_acc2", 128},
+    {"2cta_256x256_k512 (K % 256 == 0; other K run 1cta_128x256)", 256},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -307,6 +553,63 @@ nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const u
   return from_cuda(cudaGetLastError());
 }
 
+nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
+                      void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+  auto kern = pair::gemm_nvf4_pair_kernel;
+  static bool attr_set[64] = {};
+  static int max_clusters[64] = {};
+  const int d = dev.device < 64 ? dev.device : 63;
+  if (!attr_set[d]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    cudaLaunchConfig_t qc = {};
+    qc.gridDim = dim3(dev.num_sms, 1, 1);
+    qc.blockDim = dim3(pair::kThreads, 1, 1);
+    qc.dynamicSmemBytes = pair::kSmemBytes;
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = 2;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    qc.attrs = qa;
+    qc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess || n < 1) n = dev.num_sms / 2;
+    max_clusters[d] = n;
+    attr_set[d] = true;
+  }
+  CUtensorMap ta, tb, tsfa, tsfb, td;
+  // A and B as [K/256 chunks][rows][128 bytes]: one box = 128 rows x 2 chunks (K = 512).
+  nvfp4_status st = encode_tmap_u8_3d_chunks(&ta, A, M, K, 128, 2);
+  if (st == NVFP4_OK) st = encode_tmap_u8_3d_chunks(&tb, B, N, K, 128, 2);
+  // Packed scales as [bands][K/64 atoms][128 x u32]: SFA box = 8 atoms of one band,
+  // SFB box = 8 atoms of two bands.
+  if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfa, SFA, M, K, pair::kStepsP, 1);
+  if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfb, SFB, N, K, pair::kStepsP, 2);
+  if (st == NVFP4_OK)
+    st = encode_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != NVFP4_OK) return st;
+  const int tiles_m = static_cast<int>((M + 255) / 256);
+  const int tiles_n = static_cast<int>((N + 255) / 256);
+  const int num_tiles = tiles_m * tiles_n;
+  const int pairs = num_tiles < max_clusters[d] ? num_tiles : max_clusters[d];
+  const int group_n = tiles_n < 8 ? tiles_n : 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(pair::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = pair::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, tsfa, tsfb, td, alpha, static_cast<int>(K), tiles_m,
+                                      tiles_n, group_n));
+}
+
 }  // namespace
 
 int read_device_error_gemm(bool clear) {
@@ -327,8 +630,10 @@ const char* gemm_config_name(int config) {
 }
 
 int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-  (void)K;
-  // Prefer the wide tile unless it leaves most SMs idle on a small problem.
+  // CTA pairs (256 x 256 tiles, K = 512 stages) whenever the tile is filled in both
+  // dimensions and K allows the 3-D operand boxes; 128 x 256 single-CTA tiles for
+  // skinny M; 128 x 128 when N is narrow or the problem is too small to fill the SMs.
+  if (K % 256 == 0 && M > 128 && N > 128) return 3;
   const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
   if (N <= 128 || tiles256 < dev.num_sms / 2) return 2;
   return 1;
@@ -340,6 +645,9 @@ nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const
   switch (config) {
     case 1: return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
     case 2: return run<128, 4, 2>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+    case 3:
+      if (K % 256 != 0) return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+      return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
     default: return NVFP4_ERR_INVALID_ARG;
   }
 }

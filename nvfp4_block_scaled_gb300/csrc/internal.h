@@ -32,6 +32,21 @@ nvfp4_status encode_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inne
                                uint64_t row_pitch, uint32_t box_inner, uint32_t box_outer,
                                CUtensorMapSwizzle swizzle);
 
+// Same, for any element type (inner/box_inner in elements, row_pitch in bytes).
+nvfp4_status encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                            uint64_t outer, uint64_t row_pitch, uint32_t box_inner, uint32_t box_outer,
+                            CUtensorMapSwizzle swizzle);
+
+// 3-D UINT8 map over packed K-major codes [rows x K/2] viewed as [K/256][rows][128 B]
+// (128-byte swizzle); K % 256 == 0.  A box is box_rows x box_chunks 128-byte chunks.
+nvfp4_status encode_tmap_u8_3d_chunks(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows,
+                                      uint32_t box_chunks);
+
+// 3-D UINT32 map over a packed scale buffer viewed as [bands][K/64 atoms][128 words];
+// a box is box_bands x box_atoms atoms (out-of-range atoms / bands read as zero).
+nvfp4_status encode_tmap_sf_3d(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_atoms,
+                               uint32_t box_bands);
+
 // Per-translation-unit device error words (see ptx.cuh): returns the recorded
 // status (0 if none) or NVFP4_ERR_CUDA, optionally clearing it.
 int read_device_error_gemm(bool clear);

@@ -126,10 +126,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
@@ -327,8 +323,13 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* yb = static_cast<__nv_bfloat16*>(y);
   const auto* wp = static_cast<const uint8_t*>(Wprep);
-  for (int64_t m0 = 0; m0 < M; m0 += 64) {
-    const int mc = static_cast<int>(M - m0 < 64 ? M - m0 : 64);
+  // Largest token chunk (64, 32, 16 or 8 rows) whose slice of x fits in shared
+  // memory at the deepest K split.
+  int chunk = 64;
+  while (chunk > 8 && (KC % 8 != 0 || decode_smem_bytes(chunk / 8, static_cast<int>(K), 8) > dev.max_smem_optin))
+    chunk /= 2;
+  for (int64_t m0 = 0; m0 < M; m0 += chunk) {
+    const int mc = static_cast<int>(M - m0 < chunk ? M - m0 : chunk);
     const int MT = mc <= 8 ? 1 : mc <= 16 ? 2 : mc <= 32 ? 4 : 8;
     // K split: enough CTAs for about two waves, a slice of x that fits in shared memory.
     int S = 1;
