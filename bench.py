@@ -1,0 +1,495 @@
+"""Benchmark of the NVFP4 block-scaled path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+Prints ONE JSON line.  The timed step is one NVFP4 block-scaled GEMM
+D = alpha * (A*SFA)(B*SFB)^T on the square workload M = N = K = 8192 (codes
+uniform over the 16 E2M1 codes, scales uniform over the E4M3 values 2^-4..2^4,
+alpha uniform in [0.25, 4]), operands resident in HBM; L2 is flushed between
+timed iterations.  `value` is TFLOP/s (2*M*N*K per step) summed over ranks.
+Sub-measurements in the same line: the 16384^3 GEMM, the W4A16 decode GEMM
+(weight GB/s, CUDA-graph replay over rotated weight copies larger than L2) and
+the quantize / pack_scales producers (GB/s).
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload; its value is in the same unit.
+
+Under torchrun (N > 1) every rank runs the same step on its own GPU (replicas,
+weak scaling); rank 0 prints the line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 GEMM TFLOP/s at 8k/16k square, % of GB300 dense FP4 peak; W4A16 GB/s"
+FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 : BF16 tensor ratio (GB300)
+P1_V1_8K_TFLOPS = 1476.0      # pages' 8192^3 NVFP4 GEMM (RTX PRO 6000, context only)
+S_MAIN = 8192
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="skip the sub-measurements")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def all_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "", 1).isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm_w4a4.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(key)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ our arm
+
+def gemm_operands(S, seed=0):
+    import numpy as np
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+    from synthetic import generators as G
+
+    A, SFA, B, SFB = G.gemm_square_inputs(S, S, S, seed=seed)
+    alpha = G.alpha_uniform(seed)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    a, b = dev(A), dev(B)
+    sfa, sfb = nv.pack_scales(dev(SFA), S), nv.pack_scales(dev(SFB), S)
+    return (A, SFA, B, SFB, alpha), (a, sfa, b, sfb)
+
+
+def time_gemm(S, steps, warmup, world, sampler=None):
+    """Per-iteration CUDA-event time of nvfp4_gemm on S^3, L2 flushed in between."""
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+
+    host, (a, sfa, b, sfb) = gemm_operands(S)
+    alpha = host[4]
+    D = torch.empty((S, S), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        nv.gemm(a, sfa, b, sfb, alpha, S, S, S, out=D)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.zero_()                       # evict the operands from L2 (not timed)
+        e0.record(stream)
+        nv.gemm(a, sfa, b, sfb, alpha, S, S, S, out=D)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.stop()
+    barrier(world)
+    times = [e0.elapsed_time(e1) for e0, e1 in evs]
+    err = nv.device_error()
+    if err != 0:
+        raise RuntimeError(f"device error {err}")
+    return times, (host, D)
+
+
+def time_gemm_e2e(S, steps, warmup):
+    """Same GEMM through the C ABI with host buffers: H2D of A, B, SFA, SFB from pinned
+    memory, the GEMM, and D2H of D, all inside the timed region."""
+    import numpy as np
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+    from synthetic import generators as G
+
+    A, SFA, B, SFB = G.gemm_square_inputs(S, S, S, seed=0)
+    alpha = G.alpha_uniform(0)
+    # host-side packed scales (the layout the GEMM consumes) come from the GPU packer once
+    sfa_p = nv.pack_scales(torch.from_numpy(SFA).cuda(), S).cpu()
+    sfb_p = nv.pack_scales(torch.from_numpy(SFB).cuda(), S).cpu()
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hSFA = sfa_p.pin_memory()
+    hSFB = sfb_p.pin_memory()
+    hD = torch.empty((S, S), dtype=torch.bfloat16).pin_memory()
+    dA, dB = torch.empty_like(hA, device="cuda"), torch.empty_like(hB, device="cuda")
+    dSFA, dSFB = torch.empty_like(hSFA, device="cuda"), torch.empty_like(hSFB, device="cuda")
+    dD = torch.empty((S, S), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        dSFA.copy_(hSFA, non_blocking=True)
+        dSFB.copy_(hSFB, non_blocking=True)
+        nv.gemm(dA, dSFA, dB, dSFB, alpha, S, S, S, out=dD)
+        hD.copy_(dD, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hA.numel() + hB.numel() + hSFA.numel() + hSFB.numel()
+    d2h = hD.numel() * 2
+    return ms, h2d, d2h
+
+
+def bench_w4a16(peaks):
+    """W4A16 decode: weight GB/s over CUDA-graph replay of rotated weight copies."""
+    import numpy as np
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+    from synthetic import generators as G
+
+    out = {}
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    for (N, K) in [(5120, 5120), (17408, 5120), (5120, 17408)]:
+        W = G.packed_codes_uniform(N, K, 0, "W")
+        SW = G.scales_uniform_normal(N, K, 0, "SW")
+        w0 = nv.w4a16_prepare(torch.from_numpy(W).cuda(), torch.from_numpy(SW).cuda())
+        wbytes = nv.w4a16_prepared_bytes(N, K)
+        copies = max(4, int(np.ceil(4 * l2 / wbytes)))
+        ws = [w0.clone() for _ in range(copies)]
+        for M in (1, 8, 32, 72, 144, 1024):
+            x = torch.from_numpy(G.bf16_normal(M, K, 0, "x").view(np.int16)).cuda().view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            for w in ws[:2]:
+                nv.w4a16_linear(x, w, 1.0, N, out=y)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for w in ws:
+                        nv.w4a16_linear(x, w, 1.0, N, out=y, stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+            g.replay()
+            torch.cuda.synchronize()
+            best = None
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / len(ws)
+                best = us if best is None else min(best, us)
+            alg_bytes = wbytes + 2 * M * K + 2 * M * N
+            out[f"M{M}_N{N}_K{K}"] = {"us": round(best, 3), "weight_GBps": round(wbytes / best / 1e3, 1),
+                                      "GBps": round(alg_bytes / best / 1e3, 1),
+                                      "hbm_frac": round(alg_bytes / best / 1e3 / peaks["hbm_gbs"], 3),
+                                      "tflops": round(2 * M * N * K / best / 1e6, 1)}
+            del g
+        del ws
+    return out
+
+
+def bench_producers(peaks):
+    import numpy as np
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+    from synthetic import generators as G
+
+    R, K = 8192, 5120
+    x = torch.from_numpy(G.bf16_normal(R, K, 0, "x").view(np.int16)).cuda().view(torch.bfloat16)
+    codes = torch.empty((R, K // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty((R, K // 16), dtype=torch.uint8, device="cuda")
+    packed = torch.empty(nv.packed_scales_bytes(R, K), dtype=torch.uint8, device="cuda")
+    res = {}
+    for name, fn, nbytes in [
+        ("quantize", lambda: nv.quantize(x, 0.001, codes, sf), R * K * 2 + R * K // 2 + R * K // 16),
+        ("pack_scales", lambda: nv.pack_scales(sf, K, packed), 2 * R * K // 16),
+    ]:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(20):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 20
+        res[name] = {"workload": f"{R}x{K} bf16", "us": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                     "hbm_frac": round(nbytes / us / 1e3 / peaks["hbm_gbs"], 3)}
+    return res
+
+
+def cpu_baseline_gemm(S, target_s=12.0, max_samples=1 << 16):
+    """The oracle on a bounded sample of the S^3 workload: sampled outputs, each a full
+    K-length dot product of dequantised rows (float64).  Returns TFLOP/s."""
+    import numpy as np
+
+    from oracle import nvfp4_oracle as O
+    from synthetic import generators as G
+
+    A, SFA, B, SFB = G.gemm_square_inputs(S, S, S, seed=0)
+    alpha = G.alpha_uniform(0)
+    rng = np.random.default_rng(7)
+    n, total, elapsed = 64, 0, 0.0
+    while elapsed < target_s and total < max_samples:
+        rows, cols = rng.integers(0, S, n), rng.integers(0, S, n)
+        t0 = time.perf_counter()
+        O.gemm_at(A, SFA, B, SFB, alpha, rows, cols)
+        elapsed += time.perf_counter() - t0
+        total += n
+        n = min(2 * n, 4096)
+    tflops = total * 2 * S / elapsed / 1e12
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except ImportError:
+        cores = len(os.sched_getaffinity(0))
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{total} sampled outputs of the {S}^3 GEMM (full K={S} dot products, float64), {elapsed:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+
+    rank, world = dist_setup(args)
+    peaks = load_peaks()
+    S = S_MAIN
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) if rank == 0 else None
+    times, _ = time_gemm(S, args.steps, max(3, args.warmup), world, sampler)
+    ms_rank = sum(times)
+    ms_max = all_max(ms_rank, world)
+    flops = 2.0 * S ** 3
+    value = world * args.steps * flops / (ms_max / 1e3) / 1e12
+    avg_ms = statistics.mean(times)
+    achieved = flops / (avg_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": round(value / world / P1_V1_8K_TFLOPS, 3), "dtype": "nvfp4 (e2m1 x ue4m3/16) -> fp32 acc -> bf16",
+        "data": "synthetic",
+        "config": {"workload": f"NVFP4 block-scaled GEMM M=N=K={S}, A MxK and B NxK K-major, E2M1 codes uniform, "
+                               "one E4M3 scale per 16 K uniform over 2^-4..2^4, alpha U[0.25,4], BF16 out",
+                   "M": S, "N": S, "K": S, "gemm_config": torch_config_name(S),
+                   "l2": "flushed between timed iterations (512 MB write, untimed)",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(f"gemm_{S}"),
+                     "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)"},
+    }
+    if rank == 0:
+        line["clocks"] = sampler.summary() if sampler else None
+    if not args.quick:
+        t16, _ = time_gemm(16384, 3, 2, world)
+        line["gemm_16384"] = {"ms": round(statistics.mean(t16), 4),
+                              "tflops": round(2 * 16384 ** 3 / (statistics.mean(t16) / 1e3) / 1e12, 1),
+                              "frac_of_peak": round(2 * 16384 ** 3 / (statistics.mean(t16) / 1e3) / 1e12 / peak, 4)}
+        if rank == 0:
+            ms, h2d, d2h = time_gemm_e2e(S, 5, 2)
+            line["e2e"] = {"value": round(flops / (ms / 1e3) / 1e12, 1), "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                           "ms_per_step": round(ms, 3)}
+            line["w4a16"] = bench_w4a16(peaks)
+            line["producers"] = bench_producers(peaks)
+            line["cpu_baseline"] = cpu_baseline_gemm(S)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def torch_config_name(S):
+    import nvfp4_block_scaled_gb300 as nv
+
+    return nv.gemm_config_name(nv.gemm_choose_config(S, S, S))
+
+
+# ------------------------------------------------------------------ reference arm (the CPU oracle)
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    from oracle import nvfp4_oracle as O
+    from synthetic import generators as G
+
+    S = S_MAIN
+    A, SFA, B, SFB = G.gemm_square_inputs(S, S, S, seed=0)
+    alpha = G.alpha_uniform(0)
+    rng = np.random.default_rng(11)
+    n = 256  # sampled outputs per step (full K-length dot products)
+    for _ in range(args.warmup):
+        O.gemm_at(A, SFA, B, SFB, alpha, rng.integers(0, S, n), rng.integers(0, S, n))
+    times = []
+    for _ in range(args.steps):
+        rows, cols = rng.integers(0, S, n), rng.integers(0, S, n)
+        t0 = time.perf_counter()
+        O.gemm_at(A, SFA, B, SFB, alpha, rows, cols)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps * n * 2 * S / total / 1e12
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except ImportError:
+        cores = len(os.sched_getaffinity(0))
+    sample = f"{n} sampled outputs of the {S}^3 GEMM per step (float64 dot products over K={S})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"NVFP4 block-scaled GEMM M=N=K={S} (oracle on sampled outputs)", "M": S, "N": S,
+                   "K": S},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

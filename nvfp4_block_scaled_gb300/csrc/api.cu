@@ -46,6 +46,8 @@ nvfp4_status current_device(DeviceInfo* out) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess) d.cc_minor = v;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
       d.max_smem_optin = static_cast<size_t>(v);
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess)
+      d.smem_per_sm = static_cast<size_t>(v);
     d.ok = d.cc_major == 10 && d.cc_minor == 3 && d.num_sms > 0;
     g_devices[dev] = d;
   });
@@ -101,6 +103,33 @@ nvfp4_status encode_tmap_sf_3d(CUtensorMap* map, const void* base, int64_t rows,
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status encode_tmap_wprep(CUtensorMap* map, const void* wprep, int64_t N, int64_t K) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return NVFP4_ERR_CUDA;
+  const cuuint64_t dims[3] = {72, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(N / 16)};
+  const cuuint64_t strides[2] = {576, static_cast<cuuint64_t>(K / 64) * 576};
+  const cuuint32_t box[3] = {72, 8, 8};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(wprep), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+nvfp4_status encode_tmap_x_blocks(CUtensorMap* map, const void* x, int64_t M, int64_t K, uint32_t box_rows,
+                                  uint32_t box_blocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || K % 64 != 0) return NVFP4_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_blocks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -16,6 +16,7 @@ struct DeviceInfo {
   int cc_major = 0;
   int cc_minor = 0;
   size_t max_smem_optin = 0;
+  size_t smem_per_sm = 0;
   bool ok = false;  // compute capability 10.3
 };
 
@@ -46,6 +47,14 @@ nvfp4_status encode_tmap_u8_3d_chunks(CUtensorMap* map, const void* base, int64_
 // a box is box_bands x box_atoms atoms (out-of-range atoms / bands read as zero).
 nvfp4_status encode_tmap_sf_3d(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_atoms,
                                uint32_t box_bands);
+
+// 3-D UINT64 map over a prepared W4A16 weight viewed as [N/16][K/64][576 bytes];
+// a box is 8 n-tiles x 8 blocks (128 rows x 512 K, 36 KB).
+nvfp4_status encode_tmap_wprep(CUtensorMap* map, const void* wprep, int64_t N, int64_t K);
+// bf16 activations [M][K] viewed as [K/64 blocks][M tokens][64]: box = box_blocks x
+// box_rows tokens x 64, 128-byte swizzled; tokens past M read as zero.
+nvfp4_status encode_tmap_x_blocks(CUtensorMap* map, const void* x, int64_t M, int64_t K, uint32_t box_rows,
+                                  uint32_t box_blocks);
 
 // Per-translation-unit device error words (see ptx.cuh): returns the recorded
 // status (0 if none) or NVFP4_ERR_CUDA, optionally clearing it.

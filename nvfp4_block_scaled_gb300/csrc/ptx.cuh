@@ -90,6 +90,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  int ok = 1;
+  if (lane_id() == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // Wait at most `limit_ns` for a phase, ignoring the abort flag (teardown after an
 // abort: lets copies already issued land before shared memory is released).
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {

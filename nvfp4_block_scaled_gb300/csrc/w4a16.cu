@@ -7,15 +7,22 @@
 //   yields bf16x2 values fp4 * 2^-126, scales re-encoded as b with
 //   bf16(0x7000 | b<<4) = |scale| * 2^119; zero scales zero their codes, negative
 //   scales flip the code signs.  One bf16x2 multiply then gives w * 2^-7 exactly.
-// linear (decode, M <= 64 per pass): a thread block cluster of S CTAs splits K;
-//   each CTA stages its slice of x in shared memory, its 8 warps stream one
-//   16-row weight tile each straight from HBM into registers (16-byte loads,
-//   several blocks in flight), dequantise, and issue mma.sync with FP32
-//   accumulation; partial sums are reduced across the cluster through
-//   distributed shared memory in a fixed order (deterministic, no workspace),
-//   then y = bf16(acc * alpha * 2^7).
+// linear (decode, up to 32 tokens per pass): a thread block cluster of S CTAs
+//   splits K; each CTA owns 128 weight rows and a contiguous range of 512-wide K
+//   chunks.  A producer warp streams each chunk (36 KB of weights: 8 n-tiles x
+//   8 blocks, contiguous per n-tile) together with the matching x columns
+//   (Mpad tokens x 512 K, 128-byte swizzled, zero rows past M) with 3-D TMA boxes
+//   into a 2-deep ring -- large copies are what keep HBM busy; per-warp 16-byte
+//   loads top out far below it.  Sixteen consumer warps (an n-tile and half of each
+//   chunk's blocks each) dequantise from shared memory and issue mma.sync with
+//   FP32 accumulation, x fragments from ldmatrix.  Partial sums (the drained ring
+//   holds them) are reduced across the cluster through distributed shared memory in
+//   a fixed order (deterministic, no workspace), then y = bf16(acc * alpha * 2^7).
 
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cmath>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -109,28 +116,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint2 ldg_stream2(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
+// Remote (distributed shared memory) load; ordered after the preceding cluster
+// barrier by that barrier's own memory clobber.
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
   return v;
 }
 
@@ -154,133 +146,243 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t word, int idx) {
   return b * 0x00100010u + 0x70007000u;
 }
 
-constexpr int kDecodeWarps = 8;
-constexpr int kPF = 4;  // weight blocks in flight per warp
+constexpr int kDecodeNT = 8;                    // 16-row n-tiles per CTA (128 rows)
+constexpr int kDecodeWarps = 16;                // consumer warps: n-tile w % 8, chunk half w / 8
+constexpr int kDecodeThreads = 32 * (kDecodeWarps + 1);  // + one producer warp
+constexpr int kChunkKC = 8;                     // 64-wide K blocks per chunk (K = 512)
+constexpr int kChunkBytes = kDecodeNT * kChunkKC * kBlockBytes;  // 36 KB: 128 rows x 512 K
+constexpr int kRing = 2;                        // chunks in flight per CTA
+constexpr int kDecodeMaxTokens = 32;            // tokens per launch
 
+// One ring stage: the weight chunk, then x[Mpad tokens][512 K] as 8 K-blocks of
+// [Mpad][128 B] (128-byte swizzled; tokens past M are zero-filled by the copy).
+// After the main loop the ring is reused for the partial sums [2 halves][Mpad][128].
+__host__ __device__ constexpr int decode_stage_bytes(int Mpad) { return kChunkBytes + Mpad * 1024; }
+__host__ __device__ constexpr int decode_bar_off(int Mpad) { return kRing * decode_stage_bytes(Mpad); }
+// + 1 KB so the kernel can align its base to the 1024 bytes the swizzle needs.
+__host__ __device__ constexpr int decode_smem_bytes(int Mpad) { return decode_bar_off(Mpad) + 2 * kRing * 8 + 16 + 1024; }
+static_assert(2 * kDecodeMaxTokens * 128 * 4 <= kRing * kChunkBytes, "partial sums fit in the ring");
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Thread blocks per SM the register budget allows: two for up to 16 tokens.
 template <int MT>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-    w4a16_decode_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ wprep, float alpha128,
-                        __nv_bfloat16* __restrict__ y, int M, int N, int K, int S) {
+constexpr int decode_min_blocks() { return MT <= 2 ? 2 : 1; }
+
+// Weight stream: the prepared weight viewed as a 3-D tensor
+// [N/16 n-tiles][K/64 blocks][576 bytes]; one TMA box = 8 n-tiles x 8 blocks (36 KB),
+// i.e. 128 rows x 512 K, landing in shared memory as [n-tile][block][576 B].
+// Activation stream: x viewed as [K/64 blocks][M tokens][64 bf16]; one box =
+// 8 blocks x Mpad tokens, so each stage carries the x columns its chunk needs.
+template <int MT>
+__global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
+    w4a16_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                        float alpha128, __nv_bfloat16* __restrict__ y, int M, int N, int K, int S) {
   constexpr int Mpad = 8 * MT;
-  extern __shared__ __align__(16) uint8_t smem[];
+  constexpr int kStage = decode_stage_bytes(Mpad);
+  constexpr int kStageTx = kStage;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
   const int rank = blockIdx.x;  // position in the cluster = K split index
-  const int ng = blockIdx.y;    // 128-row group of N
+  const int grp = blockIdx.y;   // 128-row group of N
   const int KC = K / 64;
-  const int kc_per = KC / S;
-  const int kc0 = rank * kc_per;
-  const int Kr = kc_per * 64;
-  const int pitch = Kr + 8;  // elements; +16 bytes keeps fragment loads conflict-free
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
-  float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(Mpad) * pitch * 2);  // [Mpad][128]
+  const int C = (KC + kChunkKC - 1) / kChunkKC;
+  const int c0 = rank * C / S, c1 = (rank + 1) * C / S;
+  const int nch = c1 - c0;
+  const uint32_t ring = sbase;
+  float* part = reinterpret_cast<float*>(smem);  // [2][Mpad][128], valid after the main loop
+  const uint32_t bar_full = sbase + decode_bar_off(Mpad);
+  const uint32_t bar_empty = bar_full + 8 * kRing;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + decode_bar_off(Mpad) + 16 * kRing);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int nt = ng * kDecodeWarps + warp;
-  const uint8_t* wp = wprep + (static_cast<size_t>(nt) * KC + kc0) * kBlockBytes;
-
-  // Start the weight stream before waiting for x.
-  uint4 cw[kPF];
-  uint2 sw[kPF];
-#pragma unroll
-  for (int p = 0; p < kPF; ++p) {
-    if (p < kc_per) {
-      cw[p] = ldg_stream(wp + p * kBlockBytes + 16 * lane);
-      sw[p] = ldg_stream2(wp + p * kBlockBytes + 512 + 8 * g);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kDecodeWarps);
     }
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-
-  // Stage x[0:Mpad, kc0*64 : kc0*64 + Kr] (rows >= M zero-filled).
-  const int chunks_per_row = Kr / 8;
-  const uint32_t xs_base = smem_u32(xs);
-  for (int c = threadIdx.x; c < Mpad * chunks_per_row; c += blockDim.x) {
-    const int r = c / chunks_per_row, q = c - r * chunks_per_row;
-    const int rr = r < M ? r : 0;
-    const __nv_bfloat16* src = x + static_cast<size_t>(rr) * K + static_cast<size_t>(kc0) * 64 + q * 8;
-    cp_async16(xs_base + (r * pitch + q * 8) * 2, src, r < M ? 16u : 0u);
-  }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
-  float acc[MT][4];
+  if (warp == kDecodeWarps) {
+    // ------------------------------------------------------------ producer warp
+    if (lane == 0) {
+      prefetch_tensormap(&tmW);
+      prefetch_tensormap(&tmX);
+      for (int i = 0; i < nch; ++i) {
+        const int st = i % kRing;
+        if (i >= kRing && !mbar_wait(bar_empty + 8 * st, ((i / kRing) - 1) & 1, abort_flag)) break;
+        const uint32_t dst = ring + st * kStage;
+        mbar_arrive_expect_tx(bar_full + 8 * st, kStageTx);
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+            "l"(&tmW), "r"(0), "r"((c0 + i) * kChunkKC), "r"(grp * kDecodeNT), "r"(bar_full + 8 * st)
+            : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst + kChunkBytes),
+            "l"(&tmX), "r"(0), "r"(0), "r"((c0 + i) * kChunkKC), "r"(bar_full + 8 * st)
+            : "memory");
+      }
+      // Let every issued copy land before the thread block can exit.
+      for (int i = nch > kRing ? nch - kRing : 0; i < nch; ++i)
+        mbar_wait_for(bar_full + 8 * (i % kRing), (i / kRing) & 1, 2000000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const int nt = warp & (kDecodeNT - 1);  // n-tile within the group
+    const int half = warp / kDecodeNT;      // which half of each chunk's blocks
+    const int g = lane >> 2;
+    // ldmatrix rows: lane l supplies token 8mt + l%8 of matrix l/8, i.e. the 16-byte
+    // piece 4jj + l/8 of the token's 128-byte line, stored at piece ^ (token % 8).
+    const uint32_t row_off = static_cast<uint32_t>(lane & 7) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(lane & 7);
+    const uint32_t q = static_cast<uint32_t>(lane >> 3);
+
+    float acc[2][MT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) acc[a][mt][0] = acc[a][mt][1] = acc[a][mt][2] = acc[a][mt][3] = 0.f;
 
-  const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
-  const int pitch_w = pitch / 2;  // in 32-bit words
-
+    for (int i = 0; i < nch; ++i) {
+      const int st = i % kRing;
+      if (!warp_wait(bar_full + 8 * st, (i / kRing) & 1, abort_flag)) break;
+      const int kcc = min(kChunkKC, KC - (c0 + i) * kChunkKC);
+      const int kb0 = half * (kChunkKC / 2);
+      const int kb1 = min(kcc, kb0 + kChunkKC / 2);
+      const uint32_t stage = ring + st * kStage;
+      const uint32_t tile = stage + nt * (kChunkKC * kBlockBytes);
+      const uint32_t xstage = stage + kChunkBytes + row_off;
 #pragma unroll 1
-  for (int kc = 0; kc < kc_per; kc += kPF) {
-#pragma unroll
-    for (int p = 0; p < kPF; ++p) {
-      if (kc + p < kc_per) {
-        const uint4 c = cw[p];
-        const uint2 s = sw[p];
-        if (kc + p + kPF < kc_per) {
-          cw[p] = ldg_stream(wp + (kc + p + kPF) * kBlockBytes + 16 * lane);
-          sw[p] = ldg_stream2(wp + (kc + p + kPF) * kBlockBytes + 512 + 8 * g);
-        }
+      for (int kc = kb0; kc < kb1; ++kc) {
+        const uint32_t blk = tile + kc * kBlockBytes;
+        uint4 c;
+        uint2 sc;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
+                     : "r"(blk + 16 * lane));
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sc.x), "=r"(sc.y) : "r"(blk + 512 + 8 * g));
         const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+        const uint32_t xblk = xstage + static_cast<uint32_t>(kc * Mpad * 128);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t sword = j < 2 ? s.x : s.y;
-          const uint32_t s_lo = scale_pair(sword, (j & 1) * 2);
-          const uint32_t s_hi = scale_pair(sword, (j & 1) * 2 + 1);
-          uint32_t a[4];
-          dequant_word(words[j], s_lo, s_hi, a);
-          const int kw = ((kc + p) * 64 + 16 * j) / 2 + t;  // word column of k = 2t
+        for (int jj = 0; jj < 2; ++jj) {  // two pairs of 16-wide K steps
+          uint32_t b[MT][4];
+          const uint32_t piece = ((4u * jj + q) ^ sw) * 16u;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t* row = xw + (8 * mt + g) * pitch_w;
-            mma_bf16_16816(acc[mt], a, row[kw], row[kw + 4]);
+          for (int mt = 0; mt < MT; ++mt) ldsm_x4(xblk + mt * 1024 + piece, b[mt][0], b[mt][1], b[mt][2], b[mt][3]);
+#pragma unroll
+          for (int j2 = 0; j2 < 2; ++j2) {
+            const int j = 2 * jj + j2;
+            const uint32_t sword = j < 2 ? sc.x : sc.y;
+            const uint32_t s_lo = scale_pair(sword, (j & 1) * 2);
+            const uint32_t s_hi = scale_pair(sword, (j & 1) * 2 + 1);
+            uint32_t a[4];
+            dequant_word(words[j], s_lo, s_hi, a);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[j2][mt], a, b[mt][2 * j2], b[mt][2 * j2 + 1]);
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * st);
     }
-  }
-
-  // Partial sums -> shared memory as part[token][row in group].
-  const int rbase = warp * 16 + g;
+    // All consumers are done with the ring (every copy they waited for has landed);
+    // reuse it for the partial sums part[half][token][row in group].
+    named_bar_sync(1, 32 * kDecodeWarps);
+    float* ph = part + half * Mpad * 128;
+    const int rbase = nt * 16 + g;
+    const int t = lane & 3;
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const int tok = 8 * mt + 2 * t;
-    part[tok * 128 + rbase] = acc[mt][0];
-    part[(tok + 1) * 128 + rbase] = acc[mt][1];
-    part[tok * 128 + rbase + 8] = acc[mt][2];
-    part[(tok + 1) * 128 + rbase + 8] = acc[mt][3];
+    for (int mt = 0; mt < MT; ++mt) {
+      const int tok = 8 * mt + 2 * t;
+      ph[tok * 128 + rbase] = acc[0][mt][0] + acc[1][mt][0];
+      ph[(tok + 1) * 128 + rbase] = acc[0][mt][1] + acc[1][mt][1];
+      ph[tok * 128 + rbase + 8] = acc[0][mt][2] + acc[1][mt][2];
+      ph[(tok + 1) * 128 + rbase + 8] = acc[0][mt][3] + acc[1][mt][3];
+    }
   }
   cluster_sync_all();
 
-  // Fixed-order reduction over the cluster: this CTA finalises rows
-  // [rank*128/S, (rank+1)*128/S) of the group for every real token.
-  const int rows_per = 128 / S;
-  const uint32_t part_base = smem_u32(part);
-  for (int idx = threadIdx.x; idx < rows_per * M; idx += blockDim.x) {
-    const int tok = idx / rows_per;
-    const int row = rank * rows_per + (idx - tok * rows_per);
-    const uint32_t off = part_base + static_cast<uint32_t>(tok * 128 + row) * 4u;
+  // Fixed-order reduction over the cluster (and the two chunk halves): this CTA
+  // finalises a 1/S share of the group's 128 rows for every real token.
+  const int rows_lo = rank * 128 / S, rows_hi = (rank + 1) * 128 / S;
+  const int rows_n = rows_hi - rows_lo;
+  for (int idx = threadIdx.x; idx < rows_n * M; idx += kDecodeThreads) {
+    const int tok = idx / rows_n;
+    const int row = rows_lo + (idx - tok * rows_n);
+    const uint32_t off = sbase + static_cast<uint32_t>(tok * 128 + row) * 4u;
+    // Issue every remote load first, then add in the fixed order (rank, half).
+    float v[2 * 8];
+#pragma unroll
+    for (int src = 0; src < 8; ++src) {
+      if (src < S) {
+        v[2 * src] = ld_dsmem_f32(off, static_cast<uint32_t>(src));
+        v[2 * src + 1] = ld_dsmem_f32(off + Mpad * 128 * 4, static_cast<uint32_t>(src));
+      }
+    }
     float sum = 0.f;
-    for (int src = 0; src < S; ++src) sum += ld_dsmem_f32(off, static_cast<uint32_t>(src));
-    y[static_cast<size_t>(tok) * N + static_cast<size_t>(ng) * 128 + row] = __float2bfloat16_rn(sum * alpha128);
+#pragma unroll
+    for (int src = 0; src < 8; ++src) {
+      if (src < S) {
+        sum += v[2 * src];
+        sum += v[2 * src + 1];
+      }
+    }
+    y[static_cast<size_t>(tok) * N + static_cast<size_t>(grp) * 128 + row] = __float2bfloat16_rn(sum * alpha128);
   }
   cluster_sync_all();
 }
 
-size_t decode_smem_bytes(int MT, int K, int S) {
-  const int Kr = K / S;
-  return static_cast<size_t>(8 * MT) * (Kr + 8) * 2 + static_cast<size_t>(8 * MT) * 128 * 4;
+// K split (cluster size S) for a shape: balanced chunk counts within a cluster and
+// the thread blocks filling whole waves of the resident slots (SMs x blocks per SM).
+int choose_split(int groups, int KC, int MT, const DeviceInfo& dev) {
+  const int C = (KC + kChunkKC - 1) / kChunkKC;
+  const size_t smem = decode_smem_bytes(8 * MT);
+  int per_sm = MT <= 2 ? 2 : 1;
+  if (dev.smem_per_sm > 0) per_sm = std::min<int>(per_sm, static_cast<int>(dev.smem_per_sm / (smem + 1024)));
+  per_sm = std::max(per_sm, 1);
+  const double slots = static_cast<double>(dev.num_sms) * per_sm;
+  int best = 1;
+  double best_score = -1.0;
+  for (int S = 1; S <= 8 && S <= C; ++S) {
+    const int maxc = (C + S - 1) / S;
+    const double blocks = static_cast<double>(groups) * S;
+    const double waves = std::ceil(blocks / slots);
+    const double balance = (static_cast<double>(C) / S) / maxc;
+    const double fill = blocks / (waves * slots);
+    const double score = balance * fill;
+    if (score > best_score + 1e-9) { best_score = score; best = S; }
+  }
+  return best;
 }
 
 template <int MT>
-nvfp4_status launch_decode(const __nv_bfloat16* x, const uint8_t* wprep, float alpha128, __nv_bfloat16* y, int M,
-                           int N, int K, int S, cudaStream_t stream) {
+nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float alpha128, __nv_bfloat16* y, int M,
+                           int N, int K, int S, cudaStream_t stream, const DeviceInfo& dev) {
   auto kern = w4a16_decode_kernel<MT>;
-  const size_t smem = decode_smem_bytes(MT, K, S);
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return NVFP4_ERR_CUDA;
+  const int smem = decode_smem_bytes(8 * MT);
+  if (static_cast<size_t>(smem) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+  // The dynamic shared-memory limit is raised once per device (no per-call attribute
+  // changes, so calls can be captured in CUDA graphs).
+  static bool attr_set[64] = {};
+  const int d = dev.device < 64 ? dev.device : 63;
+  if (!attr_set[d]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    attr_set[d] = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, N / 128, 1);
-  cfg.blockDim = dim3(kDecodeWarps * 32, 1, 1);
+  cfg.blockDim = dim3(kDecodeThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -290,7 +392,7 @@ nvfp4_status launch_decode(const __nv_bfloat16* x, const uint8_t* wprep, float a
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return from_cuda(cudaLaunchKernelEx(&cfg, kern, x, wprep, alpha128, y, M, N, K, S));
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S));
 }
 
 }  // namespace
@@ -322,30 +424,25 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
   const int groups = static_cast<int>(N / 128);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* yb = static_cast<__nv_bfloat16*>(y);
-  const auto* wp = static_cast<const uint8_t*>(Wprep);
-  // Largest token chunk (64, 32, 16 or 8 rows) whose slice of x fits in shared
-  // memory at the deepest K split.
-  int chunk = 64;
-  while (chunk > 8 && (KC % 8 != 0 || decode_smem_bytes(chunk / 8, static_cast<int>(K), 8) > dev.max_smem_optin))
-    chunk /= 2;
-  for (int64_t m0 = 0; m0 < M; m0 += chunk) {
-    const int mc = static_cast<int>(M - m0 < chunk ? M - m0 : chunk);
-    const int MT = mc <= 8 ? 1 : mc <= 16 ? 2 : mc <= 32 ? 4 : 8;
-    // K split: enough CTAs for about two waves, a slice of x that fits in shared memory.
-    int S = 1;
-    while (S < 8 && KC % (2 * S) == 0 &&
-           (static_cast<int64_t>(groups) * S < 2LL * dev.num_sms ||
-            decode_smem_bytes(MT, static_cast<int>(K), S) > 100 * 1024))
-      S *= 2;
-    if (decode_smem_bytes(MT, static_cast<int>(K), S) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-    const __nv_bfloat16* xc = xb + m0 * K;
+  // The prepared weight as [N/16][K/64][576 B] (UINT64 elements: 72 per block).
+  CUtensorMap tmW;
+  {
+    nvfp4_status st = encode_tmap_wprep(&tmW, Wprep, N, K);
+    if (st != NVFP4_OK) return st;
+  }
+  // Token chunks of up to 32 rows per launch.
+  for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxTokens) {
+    const int mc = static_cast<int>(M - m0 < kDecodeMaxTokens ? M - m0 : kDecodeMaxTokens);
+    const int MT = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
+    const int S = choose_split(groups, KC, MT, dev);
+    CUtensorMap tmX;
+    nvfp4_status st = encode_tmap_x_blocks(&tmX, xb + m0 * K, mc, K, 8 * MT, kChunkKC);
+    if (st != NVFP4_OK) return st;
     __nv_bfloat16* yc = yb + m0 * N;
-    nvfp4_status st;
     switch (MT) {
-      case 1: st = launch_decode<1>(xc, wp, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream); break;
-      case 2: st = launch_decode<2>(xc, wp, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream); break;
-      case 4: st = launch_decode<4>(xc, wp, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream); break;
-      default: st = launch_decode<8>(xc, wp, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream); break;
+      case 1: st = launch_decode<1>(tmW, tmX, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
+      case 2: st = launch_decode<2>(tmW, tmX, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
+      default: st = launch_decode<4>(tmW, tmX, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
     }
     if (st != NVFP4_OK) return st;
   }
