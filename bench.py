@@ -46,6 +46,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the sub-measurements")
+    ap.add_argument("--only", choices=["w4a16", "producers"], default=None,
+                    help="run one sub-measurement alone and print its JSON (for profiling runs)")
+    ap.add_argument("--w4a16-shapes", default=None,
+                    help="with --only w4a16: comma-separated NxKxM list, e.g. 17408x5120x1")
     return ap.parse_args()
 
 
@@ -264,8 +268,13 @@ def time_gemm_e2e(S, steps, warmup):
     return ms, h2d, d2h
 
 
-def bench_w4a16(peaks):
-    """W4A16 decode: weight GB/s over CUDA-graph replay of rotated weight copies."""
+W4A16_NK = [(5120, 5120), (17408, 5120), (5120, 17408)]
+W4A16_M = (1, 8, 32, 72, 144, 1024)
+
+
+def bench_w4a16(peaks, shapes=None):
+    """W4A16 decode: weight GB/s over CUDA-graph replay of rotated weight copies.
+    shapes: list of (N, K, [M...]); default every (N, K) of W4A16_NK with every M of W4A16_M."""
     import numpy as np
     import torch
 
@@ -274,14 +283,16 @@ def bench_w4a16(peaks):
 
     out = {}
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    for (N, K) in [(5120, 5120), (17408, 5120), (5120, 17408)]:
+    if shapes is None:
+        shapes = [(N, K, W4A16_M) for (N, K) in W4A16_NK]
+    for (N, K, Ms) in shapes:
         W = G.packed_codes_uniform(N, K, 0, "W")
         SW = G.scales_uniform_normal(N, K, 0, "SW")
         w0 = nv.w4a16_prepare(torch.from_numpy(W).cuda(), torch.from_numpy(SW).cuda())
         wbytes = nv.w4a16_prepared_bytes(N, K)
         copies = max(4, int(np.ceil(4 * l2 / wbytes)))
         ws = [w0.clone() for _ in range(copies)]
-        for M in (1, 8, 32, 72, 144, 1024):
+        for M in Ms:
             x = torch.from_numpy(G.bf16_normal(M, K, 0, "x").view(np.int16)).cuda().view(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             for w in ws[:2]:
@@ -483,9 +494,28 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    import torch  # noqa: F401
+
+    peaks = load_peaks()
+    if args.only == "w4a16":
+        shapes = None
+        if args.w4a16_shapes:
+            shapes = []
+            for item in args.w4a16_shapes.split(","):
+                N, K, M = (int(v) for v in item.lower().split("x"))
+                shapes.append((N, K, (M,)))
+        out = bench_w4a16(peaks, shapes)
+    else:
+        out = bench_producers(peaks)
+    print(json.dumps({"only": args.only, "results": out}), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.only is not None and args.impl == "ours":
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
