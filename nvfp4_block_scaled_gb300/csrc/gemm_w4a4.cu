@@ -274,9 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // (two 128-byte-swizzled 16 KB sub-tiles, one per 256-wide K half), the stage's
 // scale atoms as one SFA box (8 atoms, 4 KB) and one SFB box (8 atoms of each of
 // the tile's two bands, 8 KB).  All of both CTAs' copies complete on the leader's
-// "full" barrier.  The leader's MMA thread moves the atoms into TMEM with
-// tcgen05.cp (in order with its MMAs), issues the stage's eight MMAs and releases
-// the stage to both CTAs with a multicast commit.  Eight epilogue warps per CTA
+// "full" barrier.  A scale warp of the leader moves the atoms into the stage's TMEM
+// slot with tcgen05.cp and commits to an "sf" barrier; the leader's MMA thread waits
+// for both, issues the stage's eight MMAs and releases the stage to both CTAs with a
+// multicast commit.  (The copies are the costly part of the tensor pipe's work here:
+// 24 per 8 MMAs; issuing them from their own thread lets them overlap MMA issue.)  Eight epilogue warps per CTA
 // drain the accumulator (128 lanes x 256 columns) into a 128-byte-swizzled BF16
 // staging tile, release the accumulator, and write D with TMA stores.
 namespace pair {
@@ -286,7 +288,8 @@ constexpr int kBKP = 512;                        // K per stage
 constexpr int kStepsP = kBKP / kMmaK;            // 8 MMAs per stage
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kSFWarp = kFirstEpiWarp + kEpiWarps;  // issues the scale copies into TMEM
+constexpr int kThreads = 32 * (kSFWarp + 1);
 constexpr int kABytes = 128 * (kBKP / 2);        // 32 KB: 2 sub-tiles of 128 rows x 128 B
 constexpr int kBBytes = 128 * (kBKP / 2);        // 32 KB
 constexpr int kSubTile = 128 * 128;              // 16 KB
@@ -300,7 +303,7 @@ constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
 constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 4 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
 constexpr int kOffBar = kOffOut + 4 * kOutBox;
-constexpr int kNumBars = 2 * kStages + 2;
+constexpr int kNumBars = 3 * kStages + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
@@ -327,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_empty = bar_full + 8 * kStages;     // stage released by the MMAs (both CTAs)
   const uint32_t bar_accf = bar_empty + 8 * kStages;
   const uint32_t bar_acce = bar_accf + 8;
+  const uint32_t bar_sf = bar_acce + 8;                 // stage's scales are in TMEM (leader)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
 
@@ -344,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, 2 * kEpiWarps);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -411,19 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(bar_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nk = min(kStepsP, KG - kb * kStepsP);
           const uint32_t sfa_t = tmem + kTmemSF + stage * kSFSlotCols;
           const uint32_t sfb_t = sfa_t + kSFACols;
           const uint32_t sA = sbase + kOffA + stage * kABytes;
           const uint32_t sB = sbase + kOffB + stage * kBBytes;
-          const uint32_t sSFA = sbase + kOffSFA + stage * kSFABytes;
-          const uint32_t sSFB = sbase + kOffSFB + stage * kSFBBytes;
-          for (int j = 0; j < nk; ++j) {
-            tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
-            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, make_sdesc(sSFB + j * kAtom, 0, 128, 0));
-            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, make_sdesc(sSFB + (kStepsP + j) * kAtom, 0, 128, 0));
-          }
           for (int j = 0; j < nk; ++j) {
             const uint32_t koff = (j >> 2) * kSubTile + (j & 3) * (kMmaK / 2);
             const uint64_t adesc = make_sdesc(sA + koff, 16, 1024, 2);
@@ -436,6 +435,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_commit_pair_mc(bar_accf, 0x3);
         acc_phase ^= 1;
+      }
+    }
+  } else if (warp == kSFWarp) {
+    // ------------------------------------------------------------ scale copies (leader CTA)
+    // Moves each landed stage's scale atoms into its TMEM slot (tcgen05.cp, both
+    // CTAs of the pair) and signals the MMA issuer; issued from its own thread the
+    // copies overlap the issue of the previous stage's MMAs.  The slot is free: the
+    // stage only refills (and its full barrier only completes) after the MMAs that
+    // read the slot have committed.
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const int nk = min(kStepsP, KG - kb * kStepsP);
+          const uint32_t sfa_t = tmem + kTmemSF + stage * kSFSlotCols;
+          const uint32_t sfb_t = sfa_t + kSFACols;
+          const uint32_t sSFA = sbase + kOffSFA + stage * kSFABytes;
+          const uint32_t sSFB = sbase + kOffSFB + stage * kSFBBytes;
+          for (int j = 0; j < nk; ++j) {
+            tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, make_sdesc(sSFB + j * kAtom, 0, 128, 0));
+            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, make_sdesc(sSFB + (kStepsP + j) * kAtom, 0, 128, 0));
+          }
+          tc_commit_pair_mc(bar_sf + 8 * stage, 0x1);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
       }
     }
   } else {
