@@ -1,9 +1,9 @@
 // quantize.cu -- NVFP4 operand producers: BF16 -> E2M1 codes + E4M3 block scales,
 // and the row-major -> 128x4-atom scale-factor permutation.
 //
-// Both kernels are HBM-bound elementwise/permutation kernels: one 16-element block
-// per thread (coalesced 32-byte loads, 8-byte code stores), grid sized to a
-// multiple of the SM count with a grid-stride loop.
+// Both kernels are HBM-bound: quantize takes one 16-element block per thread
+// (coalesced 32-byte loads, 8-byte code stores) over a grid sized to a multiple of
+// the SM count; pack_scales transposes 128-row bands through shared memory.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -77,28 +77,63 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
   }
 }
 
-// One thread per 32-bit word of the packed output: word w of atom a holds the
-// scales of row m = 32*(w%4) + w/4 of the atom's 128-row band, micro-blocks
-// 4*(a % groups) .. +3.  Out-of-range rows / blocks are written as zero.
+// One thread block per (128-row band, 32 atoms): the band's 128 rows x 128 scale
+// bytes are read row-major (coalesced 32-bit words) into shared memory, then
+// written out atom by atom, each atom's 128 words contiguous.  Word w of an atom
+// holds the four scales of row 32*(w%4) + w/4 of the band.  Rows past `rows` and
+// scales past C are written as zero.  The tile is XOR-swizzled on the word column
+// (by 8 * (row / 32)) so both the row-wise writes and the atom-wise reads of
+// shared memory are free of bank conflicts.
+constexpr int kPackAtoms = 32;
+constexpr int kPackPitch = kPackAtoms + 1;  // words per tile row
+
 __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restrict__ sf, int64_t rows,
-                                                          int64_t C, int64_t groups, int64_t nwords,
+                                                          int64_t C, int64_t groups, int64_t tiles_per_band,
+                                                          int64_t num_tiles, bool word_loads,
                                                           uint32_t* __restrict__ out) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nwords; i += stride) {
-    const int64_t atom = i >> 7;
-    const int w = static_cast<int>(i & 127);
-    const int64_t band = atom / groups;
-    const int64_t grp = atom - band * groups;
-    const int64_t r = band * 128 + 32 * (w & 3) + (w >> 2);
-    uint32_t v = 0;
-    if (r < rows) {
-      const uint8_t* src = sf + r * C + grp * 4;
-      const int64_t c0 = grp * 4;
+  __shared__ uint32_t tile[128 * kPackPitch];
+  for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const int64_t band = t / tiles_per_band;
+    const int64_t g0 = (t - band * tiles_per_band) * kPackAtoms;
+    const int ng = static_cast<int>(groups - g0 < kPackAtoms ? groups - g0 : kPackAtoms);
+    // Thread (row0 = tid / 32, gw = tid % 32) loads rows row0 + 8k, k = 0..15, of
+    // word column gw: sixteen independent loads in flight per thread.
+    const int gw = threadIdx.x % kPackAtoms;
+    const int row0 = threadIdx.x / kPackAtoms;
+    const int64_t c0 = 4 * (g0 + gw);
+    const bool col_ok = gw < ng;
+    if (word_loads && col_ok && c0 + 4 <= C && band * 128 + 128 <= rows) {
+      const uint8_t* src = sf + (band * 128 + row0) * C + c0;
+      uint32_t v[16];
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
-        if (c0 + b < C) v |= static_cast<uint32_t>(src[b]) << (8 * b);
+      for (int k = 0; k < 16; ++k) v[k] = __ldg(reinterpret_cast<const uint32_t*>(src + 8 * k * C));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int row = row0 + 8 * k;
+        tile[row * kPackPitch + (gw ^ (8 * (row >> 5)))] = v[k];
+      }
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < 16; ++k) {
+        const int row = row0 + 8 * k;
+        const int64_t r = band * 128 + row;
+        uint32_t w = 0;
+        if (col_ok && r < rows) {
+          const uint8_t* src = sf + r * C + c0;
+          for (int b = 0; b < 4; ++b)
+            if (c0 + b < C) w |= static_cast<uint32_t>(src[b]) << (8 * b);
+        }
+        tile[row * kPackPitch + (gw ^ (8 * (row >> 5)))] = w;
+      }
     }
-    out[i] = v;
+    __syncthreads();
+    uint32_t* dst = out + (band * groups + g0) * 128;
+    for (int i = threadIdx.x; i < ng * 128; i += blockDim.x) {
+      const int a = i >> 7, w = i & 127;
+      const int row = 32 * (w & 3) + (w >> 2);
+      dst[i] = tile[row * kPackPitch + (a ^ (8 * (row >> 5)))];
+    }
+    __syncthreads();
   }
 }
 
@@ -124,9 +159,12 @@ nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint
   const int64_t C = K / 16;
   const int64_t groups = (C + 3) / 4;
   const int64_t bands = (rows + 127) / 128;
-  const int64_t nwords = bands * groups * 128;
-  const int grid = grid_for(nwords, 256, dev, 8);
-  pack_scales_kernel<<<grid, 256, 0, stream>>>(sf, rows, C, groups, nwords, reinterpret_cast<uint32_t*>(out));
+  const bool word_loads = (C % 4 == 0) && aligned(sf, 4);
+  const int64_t tiles_per_band = (groups + kPackAtoms - 1) / kPackAtoms;
+  const int64_t num_tiles = bands * tiles_per_band;
+  const int grid = grid_for(num_tiles * 256, 256, dev, 8);
+  pack_scales_kernel<<<grid, 256, 0, stream>>>(sf, rows, C, groups, tiles_per_band, num_tiles, word_loads,
+                                               reinterpret_cast<uint32_t*>(out));
   return from_cuda(cudaGetLastError());
 }
 

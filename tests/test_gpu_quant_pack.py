@@ -22,6 +22,20 @@ def test_pack_scales_byte_exact(R, K):
     assert np.array_equal(got, want)
 
 
+def test_pack_scales_many_bands_and_unaligned_source():
+    # More (band, 32-atom) tiles than resident thread blocks (the grid-stride path),
+    # then a source one byte off a word boundary (the byte-load path).
+    R, K = 128 * 1300, 64
+    sf = G.scales_with_zero_and_subnormal(R, K, 6, "sf", 0.05, 0.05)
+    assert np.array_equal(nv.pack_scales(dev(sf), K).cpu().numpy(), O.pack_scales(sf))
+    R, K = 300, 1024
+    sf = G.scales_with_zero_and_subnormal(R, K, 8, "sf", 0.05, 0.05)
+    raw = dev(np.concatenate([np.zeros(1, np.uint8), sf.ravel()]))
+    shifted = raw[1:].view(R, K // 16)
+    assert shifted.data_ptr() % 4 != 0
+    assert np.array_equal(nv.pack_scales(shifted, K).cpu().numpy(), O.pack_scales(sf))
+
+
 @pytest.mark.parametrize("R,K,std", [(64, 512, 1.0), (300, 5120, 1.0), (128, 5120, 0.02), (8192, 5120, 1.0)])
 def test_quantize_byte_exact(R, K, std):
     x = G.bf16_normal(R, K, 7, "x", std)
