@@ -197,6 +197,17 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D(tmem, FP32) (+)= A(smem) x B(smem)^T for BF16 operands (kind::f16).
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit TMEM -> 32 registers per thread (thread i = lane i).
 __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

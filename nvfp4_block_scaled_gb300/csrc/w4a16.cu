@@ -7,7 +7,9 @@
 //   yields bf16x2 values fp4 * 2^-126, scales re-encoded as b with
 //   bf16(0x7000 | b<<4) = |scale| * 2^119; zero scales zero their codes, negative
 //   scales flip the code signs.  One bf16x2 multiply then gives w * 2^-7 exactly.
-// linear (decode, up to 32 tokens per pass): a thread block cluster of S CTAs
+// linear, more than 32 tokens: weights dequantised into shared memory, tcgen05
+//   kind::f16 MMAs with the tokens as the N dimension (see the tensor-core section).
+// linear, up to 32 tokens (decode): a thread block cluster of S CTAs
 //   splits K; each CTA owns 128 weight rows and a contiguous range of 512-wide K
 //   chunks.  A producer warp streams each chunk (36 KB of weights: 8 n-tiles x
 //   8 blocks, contiguous per n-tile) together with the matching x columns
@@ -123,6 +125,16 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote));
   return v;
 }
 
@@ -395,6 +407,367 @@ nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S));
 }
 
+// ------------------------------------------------------------------ linear (tensor cores)
+//
+// For more than 32 tokens the weights are dequantised into shared memory and the
+// products run on the tcgen05 tensor cores (kind::f16: BF16 x BF16 -> FP32 in TMEM):
+// the 128 weight rows of a group are the MMA's M dimension, the tokens (up to 256
+// per tile) its N dimension, so every dequantised weight feeds all tokens at once.
+//   warp 0      TMA: 36 KB prepared-weight chunks (128 rows x 512 K) into a 2-deep ring
+//   warp 1      TMA: x tiles (tokens x 64 K, 128-byte swizzled, zero rows past M)
+//   warp 2      TMEM allocation; lane 0 issues the MMAs (4 x K=16 per 64-K block)
+//   warps 3-18  dequantise: warp (p, w) turns n-tile w's 576-byte block of each
+//               64-K step i with i % 2 == p into rows 16w..16w+15 of a 128 x 64 BF16
+//               A tile (128-byte swizzle, the layout the MMA's K-major descriptor
+//               reads)
+//   warps 3-6   epilogue: TMEM -> registers -> y (or, when a cluster splits K, ->
+//               shared memory, fixed-order reduction across the cluster through
+//               distributed shared memory -> y)
+namespace tcw {
+
+constexpr int kMaxRawStages = 4;
+constexpr int kMaxAStages = 4;
+constexpr int kMaxXStages = 16;
+constexpr int kABytes = 128 * 128;                // 128 rows x 64 K bf16
+constexpr int kDeqWarps = 16;                     // two groups of 8: even and odd 64-K steps
+constexpr int kFirstDeqWarp = 3;
+constexpr int kThreads = 32 * (kFirstDeqWarp + kDeqWarps);
+constexpr int kMaxTokens = 256;
+constexpr int kNumBars = 2 * kMaxRawStages + 2 * kMaxAStages + 2 * kMaxXStages + 1;
+
+// Shared memory: a ring of 36 KB weight chunks, dequantised A tiles and x tiles.
+// The weight ring is what keeps HBM busy (a chunk takes several microseconds to
+// arrive under load), the A ring decouples dequantisation from the MMAs, and an x
+// slot refills only after the MMA that read it has completed.  Minimums first
+// (2 chunks, 3 A tiles, 3 x tiles), then chunks up to 4, then x tiles up to 16.
+struct Layout {
+  int rs, as, xs;
+  int off_a, off_x, off_bar, total;
+};
+
+__host__ __device__ inline Layout layout(int nt) {
+  Layout L;
+  const int xbytes = nt * 128;
+  const int budget = 232448 - 1024 - 8 * kNumBars - 16;
+  L.as = 3;
+  L.xs = 3;
+  L.rs = (budget - L.as * kABytes - L.xs * xbytes) / kChunkBytes;
+  if (L.rs > kMaxRawStages) L.rs = kMaxRawStages;
+  L.xs = (budget - L.as * kABytes - L.rs * kChunkBytes) / xbytes;
+  if (L.xs > kMaxXStages) L.xs = kMaxXStages;
+  L.off_a = L.rs * kChunkBytes;
+  L.off_x = L.off_a + L.as * kABytes;
+  L.off_bar = L.off_x + L.xs * xbytes;
+  L.total = L.off_bar + 8 * kNumBars + 16 + 1024;
+  return L;
+}
+
+__host__ __device__ inline uint32_t tmem_cols_for(int nt) {
+  return nt <= 32 ? 32u : nt <= 64 ? 64u : nt <= 128 ? 128u : 256u;
+}
+
+// kind::f16 instruction descriptor: FP32 accumulator (bits 4-5 = 1), A and B BF16
+// (bits 7-9 and 10-12 = 1), both K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    float alpha128, __nv_bfloat16* __restrict__ y, int M, int N, int K, int S, int nt_tok) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  const Layout L = layout(nt_tok);
+  const int rank = blockIdx.x;  // K split index (position in the cluster)
+  const int grp = blockIdx.y;   // 128-row group of N
+  const int m0 = blockIdx.z * nt_tok;
+  const int KC = K / 64;
+  const int C = (KC + kChunkKC - 1) / kChunkKC;
+  const int c0 = rank * C / S, c1 = (rank + 1) * C / S;
+  const int ks0 = c0 * kChunkKC, ks1 = min(c1 * kChunkKC, KC);  // 64-K steps of this rank
+  const int xbytes = nt_tok * 128;
+
+  const uint32_t raw_full = sbase + L.off_bar;
+  const uint32_t raw_empty = raw_full + 8 * kMaxRawStages;
+  const uint32_t a_full = raw_empty + 8 * kMaxRawStages;
+  const uint32_t a_empty = a_full + 8 * kMaxAStages;
+  const uint32_t x_full = a_empty + 8 * kMaxAStages;
+  const uint32_t x_empty = x_full + 8 * kMaxXStages;
+  const uint32_t acc_full = x_empty + 8 * kMaxXStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_bar + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 8 * kNumBars + 4);
+  const int AS = L.as;
+  const int RS = L.rs;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ncols = tmem_cols_for(nt_tok);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(raw_full + 8 * i, 1);
+      mbar_init(raw_empty + 8 * i, kDeqWarps);
+    }
+    for (int i = 0; i < AS; ++i) {
+      mbar_init(a_full + 8 * i, kDeqWarps / 2);
+      mbar_init(a_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < L.xs; ++i) {
+      mbar_init(x_full + 8 * i, 1);
+      mbar_init(x_empty + 8 * i, 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ weight chunks
+    if (lane == 0) {
+      prefetch_tensormap(&tmW);
+      const int nch = c1 - c0;
+      for (int i = 0; i < nch; ++i) {
+        const int st = i % RS;
+        if (i >= RS && !mbar_wait(raw_empty + 8 * st, ((i / RS) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(raw_full + 8 * st, kChunkBytes);
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + st * kChunkBytes),
+            "l"(&tmW), "r"(0), "r"((c0 + i) * kChunkKC), "r"(grp * kDecodeNT), "r"(raw_full + 8 * st)
+            : "memory");
+      }
+      for (int i = nch > RS ? nch - RS : 0; i < nch; ++i)
+        mbar_wait_for(raw_full + 8 * (i % RS), (i / RS) & 1, 2000000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ x tiles
+    if (lane == 0) {
+      prefetch_tensormap(&tmX);
+      const int n = ks1 - ks0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % L.xs;
+        if (i >= L.xs && !mbar_wait(x_empty + 8 * st, ((i / L.xs) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(x_full + 8 * st, xbytes);
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + L.off_x + st * xbytes),
+            "l"(&tmX), "r"(0), "r"(m0), "r"(ks0 + i), "r"(x_full + 8 * st)
+            : "memory");
+      }
+      for (int i = n > L.xs ? n - L.xs : 0; i < n; ++i)
+        mbar_wait_for(x_full + 8 * (i % L.xs), (i / L.xs) & 1, 2000000000ull);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, nt_tok);
+      const int n = ks1 - ks0;
+      for (int i = 0; i < n; ++i) {
+        const int as = i % AS, xs = i % L.xs;
+        if (!mbar_wait(a_full + 8 * as, (i / AS) & 1, abort_flag)) break;
+        if (!mbar_wait(x_full + 8 * xs, (i / L.xs) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t sa = sbase + L.off_a + as * kABytes;
+        const uint32_t sx = sbase + L.off_x + xs * xbytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc_mma_f16(tmem, make_sdesc(sa + 32 * k, 16, 1024, 2), make_sdesc(sx + 32 * k, 16, 1024, 2), idesc,
+                     (i | k) != 0 ? 1u : 0u);
+        tc_commit(a_empty + 8 * as);
+        tc_commit(x_empty + 8 * xs);
+      }
+      tc_commit(acc_full);
+    }
+  } else {
+    // ------------------------------------------------------------ dequantise
+    // Warp (p, w): n-tile w of every step i with i % 2 == p -- two steps in flight,
+    // since one block per warp is a short dependent chain that latency, not issue,
+    // bounds.
+    const int w = (warp - kFirstDeqWarp) & 7;     // n-tile within the group
+    const int par = (warp - kFirstDeqWarp) >> 3;  // step parity handled by this warp
+    const int g = lane >> 2, t = lane & 3;
+    const int n = ks1 - ks0;
+    for (int i = par; i < n; i += 2) {
+      const int kb = i % kChunkKC;        // block within the chunk
+      const int ci = i / kChunkKC;        // chunk index (relative)
+      const int rs = ci % RS;
+      const int as = i % AS;
+      if (kb == par && !warp_wait(raw_full + 8 * rs, (ci / RS) & 1, abort_flag)) break;
+      if (i >= AS && !warp_wait(a_empty + 8 * as, ((i / AS) - 1) & 1, abort_flag)) break;
+      const uint32_t blk = sbase + rs * kChunkBytes + (w * kChunkKC + kb) * kBlockBytes;
+      uint4 c;
+      uint2 sc;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
+                   : "r"(blk + 16 * lane));
+      asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sc.x), "=r"(sc.y) : "r"(blk + 512 + 8 * g));
+      const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+      // Rows 16w + g and 16w + g + 8 of the A tile; row r's 16-byte piece p sits at
+      // r * 128 + ((p ^ (r % 8)) * 16) (128-byte swizzle), and r % 8 == g here.
+      const uint32_t a_lo = sbase + L.off_a + as * kABytes + (16 * w + g) * 128 + 4 * t;
+      const uint32_t a_hi = a_lo + 8 * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sword = j < 2 ? sc.x : sc.y;
+        uint32_t a[4];
+        dequant_word(words[j], scale_pair(sword, (j & 1) * 2), scale_pair(sword, (j & 1) * 2 + 1), a);
+        const uint32_t p0 = static_cast<uint32_t>(((2 * j) ^ g) * 16);
+        const uint32_t p1 = static_cast<uint32_t>(((2 * j + 1) ^ g) * 16);
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_lo + p0), "r"(a[0]) : "memory");
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_hi + p0), "r"(a[1]) : "memory");
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_lo + p1), "r"(a[2]) : "memory");
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_hi + p1), "r"(a[3]) : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(a_full + 8 * as);
+        // Last step of this parity in the chunk: the chunk's blocks of this warp are
+        // consumed.  (A warp with no step in a partial last chunk never arrives for
+        // it; nothing waits for that phase.)
+        if (kb + 2 >= kChunkKC || i + 2 >= n) mbar_arrive(raw_empty + 8 * rs);
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue (warps 3-6)
+    if (warp - kFirstDeqWarp < 4) {
+      const int q = warp & 3;  // TMEM lane quarter this warp may access
+      const int row = 32 * q + lane;
+      const int mv = min(nt_tok, M - m0);
+      if (warp_wait(acc_full, 0, abort_flag)) {
+        tc_fence_after();
+        float* part = reinterpret_cast<float*>(smem);  // [tokens][128 rows], after the loop
+#pragma unroll 1
+        for (int c32 = 0; c32 < nt_tok; c32 += 32) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c32, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int tok = c32 + jj;
+            if (tok < mv) {
+              if (S == 1)
+                y[static_cast<size_t>(m0 + tok) * N + static_cast<size_t>(grp) * 128 + row] =
+                    __float2bfloat16_rn(__uint_as_float(v[jj]) * alpha128);
+              else
+                part[tok * 128 + row] = __uint_as_float(v[jj]);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  if (S > 1) {
+    // Fixed-order reduction over the cluster: this CTA finalises a 1/S share of the
+    // group's 128 rows (in units of 4 rows: one 16-byte remote load per source) for
+    // every token of the tile.
+    cluster_sync_all();
+    const int mv = min(nt_tok, M - m0);
+    const int q_lo = rank * 32 / S, q_hi = (rank + 1) * 32 / S;
+    const int q_n = q_hi - q_lo;
+    for (int idx = threadIdx.x; idx < q_n * mv; idx += kThreads) {
+      const int tok = idx / q_n;
+      const int row = 4 * (q_lo + (idx - tok * q_n));
+      const uint32_t off = sbase + static_cast<uint32_t>(tok * 128 + row) * 4u;
+      float4 v[8];
+#pragma unroll
+      for (int src = 0; src < 8; ++src)
+        if (src < S) v[src] = ld_dsmem_f32x4(off, static_cast<uint32_t>(src));
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int src = 0; src < 8; ++src) {
+        if (src < S) {
+          sum.x += v[src].x;
+          sum.y += v[src].y;
+          sum.z += v[src].z;
+          sum.w += v[src].w;
+        }
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x * alpha128, sum.y * alpha128);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z * alpha128, sum.w * alpha128);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(y + static_cast<size_t>(m0 + tok) * N + static_cast<size_t>(grp) * 128 + row) = packed;
+    }
+    cluster_sync_all();
+  }
+  if (warp == 2) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+}  // namespace tcw
+
+// Split count S (cluster size) and token-tile width for the tensor-core path: tiles
+// = groups x token tiles; S <= 8 splits K when the tiles alone leave SMs idle.
+void choose_tc(int groups, int KC, int M, const DeviceInfo& dev, int* S_out, int* nt_out, int* ttiles_out) {
+  const int mt = (M + tcw::kMaxTokens - 1) / tcw::kMaxTokens;     // token tiles
+  const int per = (M + mt - 1) / mt;
+  const int nt = ((per + 15) / 16) * 16;                          // tokens per tile (multiple of 16)
+  const int C = (KC + kChunkKC - 1) / kChunkKC;
+  const double slots = dev.num_sms;
+  int best = 1;
+  double best_score = -1.0;
+  for (int S = 1; S <= 8 && S <= C; ++S) {
+    const int maxc = (C + S - 1) / S;
+    const double blocks = static_cast<double>(groups) * mt * S;
+    const double waves = std::ceil(blocks / slots);
+    const double score = ((static_cast<double>(C) / S) / maxc) * (blocks / (waves * slots)) / (1.0 + 0.02 * (S - 1));
+    if (score > best_score + 1e-9) { best_score = score; best = S; }
+  }
+  *S_out = best;
+  *nt_out = nt;
+  *ttiles_out = mt;
+}
+
+nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, __nv_bfloat16* y, int M, int N, int K,
+                       cudaStream_t stream, const DeviceInfo& dev) {
+  int S, nt, mt;
+  choose_tc(N / 128, K / 64, M, dev, &S, &nt, &mt);
+  const tcw::Layout L = tcw::layout(nt);
+  if (L.rs < 2 || L.xs < 3 || static_cast<size_t>(L.total) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (S > 1 && nt * 128 * 4 > L.off_bar) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap tmX;
+  nvfp4_status st = encode_tmap_x_blocks(&tmX, x, M, K, static_cast<uint32_t>(nt), 1);
+  if (st != NVFP4_OK) return st;
+  auto kern = tcw::w4a16_tc_kernel;
+  static bool attr_set[64] = {};
+  const int d = dev.device < 64 ? dev.device : 63;
+  if (!attr_set[d]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dev.max_smem_optin)) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    attr_set[d] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, N / 128, mt);
+  cfg.blockDim = dim3(tcw::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S, nt));
+}
+
 }  // namespace
 
 int read_device_error_w4a16(bool clear) {
@@ -430,6 +803,13 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
     nvfp4_status st = encode_tmap_wprep(&tmW, Wprep, N, K);
     if (st != NVFP4_OK) return st;
   }
+  // More than 32 tokens: tensor cores (dequantise once into shared memory, every
+  // weight feeding all tokens).  Up to 32 tokens: the register-dequant decode kernel,
+  // which streams at a higher rate there -- the tensor-core path recycles each A
+  // tile through an MMA commit (about a microsecond), and shared memory holds too
+  // few tiles to hide that at decode-sized MMAs.
+  if (M > 32) return launch_tc(tmW, xb, alpha128, yb, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
+                               stream, dev);
   // Token chunks of up to 32 rows per launch.
   for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxTokens) {
     const int mc = static_cast<int>(M - m0 < kDecodeMaxTokens ? M - m0 : kDecodeMaxTokens);

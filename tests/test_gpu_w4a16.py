@@ -47,6 +47,23 @@ def test_linear_small_full(M):
     assert_within(host_f64(y), ref, abs_sum, alpha, f"w4a16 M={M}")
 
 
+@pytest.mark.parametrize("M,N,K", [(40, 384, 768), (24, 256, 4096), (200, 128, 1280), (300, 256, 512)])
+def test_linear_tensor_core_edges(M, N, K):
+    # Ragged K (last weight chunk partly outside the tensor), many K chunks for few
+    # rows (the K split across a cluster with its fixed-order reduction), and token
+    # counts above one 256-token tile.
+    x = G.bf16_normal(M, K, M + K, "x")
+    W = G.packed_codes_uniform(N, K, M + K, "W")
+    SW = G.scales_with_zero_and_subnormal(N, K, M + K, "SW", 0.05, 0.05)
+    alpha = 1.25
+    wp = nv.w4a16_prepare(dev(W), dev(SW))
+    y = nv.w4a16_linear(dev_bf16(x), wp, alpha, N)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    ref, abs_sum = O.w4a16_linear(x, W, SW, alpha)
+    assert_within(host_f64(y), ref, abs_sum, alpha, f"w4a16 {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("N,K", [(5120, 5120), (17408, 5120), (5120, 17408)])
 @pytest.mark.parametrize("M", [1, 8, 32, 72, 144, 1024])
 def test_linear_decode_shapes(M, N, K):
