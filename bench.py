@@ -317,11 +317,25 @@ def bench_w4a16(peaks, shapes=None):
                 torch.cuda.synchronize()
                 us = e0.elapsed_time(e1) * 1e3 / len(ws)
                 best = us if best is None else min(best, us)
+            # one call alone (weights not in L2, no call before or after it); a short
+            # device-side sleep queued first keeps the host's launch cost out of the
+            # event interval, so this is the call's device time
+            iso = []
+            for i in range(min(len(ws), 8)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                torch.cuda._sleep(200000)
+                e0.record()
+                nv.w4a16_linear(x, ws[i], 1.0, N, out=y)
+                e1.record()
+                torch.cuda.synchronize()
+                iso.append(e0.elapsed_time(e1) * 1e3)
             alg_bytes = wbytes + 2 * M * K + 2 * M * N
             out[f"M{M}_N{N}_K{K}"] = {"us": round(best, 3), "weight_GBps": round(wbytes / best / 1e3, 1),
                                       "GBps": round(alg_bytes / best / 1e3, 1),
                                       "hbm_frac": round(alg_bytes / best / 1e3 / peaks["hbm_gbs"], 3),
-                                      "tflops": round(2 * M * N * K / best / 1e6, 1)}
+                                      "tflops": round(2 * M * N * K / best / 1e6, 1),
+                                      "isolated_us": round(statistics.median(iso), 2)}
             del g
         del ws
     return out

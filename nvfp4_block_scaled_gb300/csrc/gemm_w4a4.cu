@@ -267,34 +267,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64 per instruction).  Each CTA
 // stages its own 128 rows of A and its own 128 rows of B.
 //
-// Operand delivery is organised around the copy engine: on this GPU an SM's TMA
-// engine sustains far more bytes per cycle with large boxes (a 16 KB box moves
-// ~24 B/clk per SM under load, a 32 KB box ~60 B/clk).  So a pipeline stage
-// covers K = 512 and every copy is large: A and B arrive as one 32 KB 3-D box each
-// (two 128-byte-swizzled 16 KB sub-tiles, one per 256-wide K half), the stage's
-// scale atoms as one SFA box (8 atoms, 4 KB) and one SFB box (8 atoms of each of
-// the tile's two bands, 8 KB).  All of both CTAs' copies complete on the leader's
-// "full" barrier.  A scale warp of the leader moves the atoms into the stage's TMEM
+// Operand delivery: under load a TMA copy takes about 1.4 us to land, so what
+// bounds the feed is the number of bytes in flight, and shared memory caps that.
+// Four stages of K = 256 keep three stages (about 1.6 us of MMA work) in flight
+// while one is consumed; two stages of K = 512 (the same bytes) covered only one
+// and measured 6-8 % slower at 8192^3 and 16384^3.  Per stage A and B arrive as
+// one 16 KB box each (128 rows x 128 bytes, 128-byte swizzle), the scale atoms as
+// one SFA box (4 atoms, 2 KB) and one SFB box (4 atoms of each of the tile's two
+// bands, 4 KB).  All of both CTAs' copies complete on the leader's "full" barrier.  A scale warp of the leader moves the atoms into the stage's TMEM
 // slot with tcgen05.cp and commits to an "sf" barrier; the leader's MMA thread waits
 // for both, issues the stage's eight MMAs and releases the stage to both CTAs with a
 // multicast commit.  (The copies are the costly part of the tensor pipe's work here:
-// 24 per 8 MMAs; issuing them from their own thread lets them overlap MMA issue.)  Eight epilogue warps per CTA
+// 12 per 4 MMAs; issuing them from their own thread lets them overlap MMA issue.)  Eight epilogue warps per CTA
 // drain the accumulator (128 lanes x 256 columns) into a 128-byte-swizzled BF16
 // staging tile, release the accumulator, and write D with TMA stores.
 namespace pair {
 
-constexpr int kStages = 2;
-constexpr int kBKP = 512;                        // K per stage
-constexpr int kStepsP = kBKP / kMmaK;            // 8 MMAs per stage
+constexpr int kStages = 4;
+constexpr int kBKP = 256;                        // K per stage
+constexpr int kStepsP = kBKP / kMmaK;            // 4 MMAs per stage
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2;
 constexpr int kSFWarp = kFirstEpiWarp + kEpiWarps;  // issues the scale copies into TMEM
 constexpr int kThreads = 32 * (kSFWarp + 1);
-constexpr int kABytes = 128 * (kBKP / 2);        // 32 KB: 2 sub-tiles of 128 rows x 128 B
-constexpr int kBBytes = 128 * (kBKP / 2);        // 32 KB
+constexpr int kABytes = 128 * (kBKP / 2);        // 16 KB: 128 rows x 128 B
+constexpr int kBBytes = 128 * (kBKP / 2);        // 16 KB
 constexpr int kSubTile = 128 * 128;              // 16 KB
-constexpr int kSFABytes = kStepsP * kAtom;       // 4 KB
-constexpr int kSFBBytes = 2 * kStepsP * kAtom;   // 8 KB: [band][atom]
+constexpr int kSFABytes = kStepsP * kAtom;       // 2 KB
+constexpr int kSFBBytes = 2 * kStepsP * kAtom;   // 4 KB: [band][atom]
 constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
@@ -386,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
           const uint32_t fb = full_leader + 8 * stage;
-          tma_load_3d_pair(sbase + kOffA + stage * kABytes, &tmA, fb, 0, a_row, 2 * kb);
-          tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, 2 * kb);
+          tma_load_3d_pair(sbase + kOffA + stage * kABytes, &tmA, fb, 0, a_row, (kBKP / 256) * kb);
+          tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * kb);
           tma_load_3d_pair(sbase + kOffSFA + stage * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
                            mt * 2 + static_cast<int>(rank));
           tma_load_3d_pair(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, kb * kStepsP, nt * 2);
@@ -544,7 +544,7 @@ struct ConfigEntry {
 constexpr ConfigEntry kConfigs[] = {
     {"1cta_128x256_s3_acc1", 256},
     {"1cta_128x128_s4_acc2", 128},
-    {"2cta_256x256_k512 (K % 256 == 0; other K run 1cta_128x256)", 256},
+    {"2cta_256x256_k256x4 (K % 256 == 0; other K run 1cta_128x256)", 256},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -601,11 +601,11 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
     attr_set[d] = true;
   }
   CUtensorMap ta, tb, tsfa, tsfb, td;
-  // A and B as [K/256 chunks][rows][128 bytes]: one box = 128 rows x 2 chunks (K = 512).
-  nvfp4_status st = encode_tmap_u8_3d_chunks(&ta, A, M, K, 128, 2);
-  if (st == NVFP4_OK) st = encode_tmap_u8_3d_chunks(&tb, B, N, K, 128, 2);
-  // Packed scales as [bands][K/64 atoms][128 x u32]: SFA box = 8 atoms of one band,
-  // SFB box = 8 atoms of two bands.
+  // A and B as [K/256 chunks][rows][128 bytes]: one box = 128 rows x one stage's chunks.
+  nvfp4_status st = encode_tmap_u8_3d_chunks(&ta, A, M, K, 128, pair::kBKP / 256);
+  if (st == NVFP4_OK) st = encode_tmap_u8_3d_chunks(&tb, B, N, K, 128, pair::kBKP / 256);
+  // Packed scales as [bands][K/64 atoms][128 x u32]: SFA box = one stage's atoms of one
+  // band, SFB box = one stage's atoms of two bands.
   if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfa, SFA, M, K, pair::kStepsP, 1);
   if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfb, SFB, N, K, pair::kStepsP, 2);
   if (st == NVFP4_OK)
@@ -652,7 +652,7 @@ const char* gemm_config_name(int config) {
 }
 
 int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-  // CTA pairs (256 x 256 tiles, K = 512 stages) whenever the tile is filled in both
+  // CTA pairs (256 x 256 tiles, four K = 256 stages) whenever the tile is filled in both
   // dimensions and K allows the 3-D operand boxes; 128 x 256 single-CTA tiles for
   // skinny M; 128 x 128 when N is narrow or the problem is too small to fill the SMs.
   if (K % 256 == 0 && M > 128 && N > 128) return 3;

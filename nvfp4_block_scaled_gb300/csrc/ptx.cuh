@@ -108,6 +108,19 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uin
   return true;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Block until every grid this one depends on (the previous kernel in the stream,
+// when this one was launched with programmatic stream serialization) has completed
+// and its memory operations are visible.  Returns at once when there is none.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next programmatically dependent grid in the stream to start launching
+// (it still waits for this grid's completion at its own griddep_wait()).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA / bulk copies
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

@@ -222,27 +222,43 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
     fence_mbar_init();
   }
   __syncthreads();
+  // The next call in the stream may start its weight stream now (see below).
+  griddep_launch_dependents();
 
   if (warp == kDecodeWarps) {
     // ------------------------------------------------------------ producer warp
     if (lane == 0) {
       prefetch_tensormap(&tmW);
       prefetch_tensormap(&tmX);
-      for (int i = 0; i < nch; ++i) {
+      auto load_w = [&](int i) {
         const int st = i % kRing;
-        if (i >= kRing && !mbar_wait(bar_empty + 8 * st, ((i / kRing) - 1) & 1, abort_flag)) break;
-        const uint32_t dst = ring + st * kStage;
         mbar_arrive_expect_tx(bar_full + 8 * st, kStageTx);
         asm volatile(
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(ring + st * kStage),
             "l"(&tmW), "r"(0), "r"((c0 + i) * kChunkKC), "r"(grp * kDecodeNT), "r"(bar_full + 8 * st)
             : "memory");
+      };
+      auto load_x = [&](int i) {
+        const int st = i % kRing;
         asm volatile(
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst + kChunkBytes),
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(ring + st * kStage + kChunkBytes),
             "l"(&tmX), "r"(0), "r"(0), "r"((c0 + i) * kChunkKC), "r"(bar_full + 8 * st)
             : "memory");
+      };
+      // The weights never depend on an earlier kernel: the first ring stages' chunks
+      // are requested before waiting for the previous grid in the stream, which may
+      // be producing x (with programmatic launch this overlaps its tail).
+      const int npre = nch < kRing ? nch : kRing;
+      for (int i = 0; i < npre; ++i) load_w(i);
+      griddep_wait();
+      for (int i = 0; i < npre; ++i) load_x(i);
+      for (int i = npre; i < nch; ++i) {
+        const int st = i % kRing;
+        if (!mbar_wait(bar_empty + 8 * st, ((i / kRing) - 1) & 1, abort_flag)) break;
+        load_w(i);
+        load_x(i);
       }
       // Let every issued copy land before the thread block can exit.
       for (int i = nch > kRing ? nch - kRing : 0; i < nch; ++i)
@@ -250,6 +266,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
     }
   } else {
     // ------------------------------------------------------------ consumer warps
+    // Start the (time-limited) barrier waits only once the previous grid is done.
+    griddep_wait();
     const int nt = warp & (kDecodeNT - 1);  // n-tile within the group
     const int half = warp / kDecodeNT;      // which half of each chunk's blocks
     const int g = lane >> 2;
@@ -322,6 +340,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
       ph[(tok + 1) * 128 + rbase + 8] = acc[0][mt][3] + acc[1][mt][3];
     }
   }
+  griddep_wait();  // y may still be written by the previous grid in the stream
   cluster_sync_all();
 
   // Fixed-order reduction over the cluster (and the two chunk halves): this CTA
@@ -397,13 +416,18 @@ nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: the kernel may start before the previous one in
+  // the stream has finished; it waits for it (griddepcontrol.wait) before reading x
+  // or writing y, and streams its weights meanwhile.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S));
 }
 
@@ -528,14 +552,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight chunks
+    // The first ring's chunks are requested before waiting for the previous grid in
+    // the stream (the weights never depend on it); every time-limited wait comes after.
     if (lane == 0) {
       prefetch_tensormap(&tmW);
       const int nch = c1 - c0;
       for (int i = 0; i < nch; ++i) {
         const int st = i % RS;
+        if (i == RS) griddep_wait();
         if (i >= RS && !mbar_wait(raw_empty + 8 * st, ((i / RS) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(raw_full + 8 * st, kChunkBytes);
         asm volatile(
@@ -551,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ x tiles
     if (lane == 0) {
       prefetch_tensormap(&tmX);
+      griddep_wait();  // x may be produced by the previous grid in the stream
       const int n = ks1 - ks0;
       for (int i = 0; i < n; ++i) {
         const int st = i % L.xs;
@@ -568,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      griddep_wait();
       const uint32_t idesc = idesc_bf16(128, nt_tok);
       const int n = ks1 - ks0;
       for (int i = 0; i < n; ++i) {
@@ -591,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warp (p, w): n-tile w of every step i with i % 2 == p -- two steps in flight,
     // since one block per warp is a short dependent chain that latency, not issue,
     // bounds.
+    griddep_wait();
     const int w = (warp - kFirstDeqWarp) & 7;     // n-tile within the group
     const int par = (warp - kFirstDeqWarp) >> 3;  // step parity handled by this warp
     const int g = lane >> 2, t = lane & 3;
@@ -672,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Fixed-order reduction over the cluster: this CTA finalises a 1/S share of the
     // group's 128 rows (in units of 4 rows: one 16-byte remote load per source) for
     // every token of the tile.
+    griddep_wait();
     cluster_sync_all();
     const int mv = min(nt_tok, M - m0);
     const int q_lo = rank * 32 / S, q_hi = (rank + 1) * 32 / S;
@@ -758,13 +790,15 @@ nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, __
   cfg.blockDim = dim3(tcw::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as in launch_decode
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S, nt));
 }
 

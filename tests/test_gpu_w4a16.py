@@ -95,3 +95,81 @@ def test_linear_repeat_is_bit_identical(M):
     y2 = nv.w4a16_linear(x, wp, g, N)
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def _chain_inputs(M, seed):
+    # Two layers: x [M x 5120] -> W1 (N=1024, K=5120) -> y1 [M x 1024] -> W2 (N=5120, K=1024).
+    x = dev_bf16(G.bf16_normal(M, 5120, seed, "x"))
+    W1, SW1, g1 = quantized_weight(1024, 5120, seed)
+    W2, SW2, g2 = quantized_weight(5120, 1024, seed + 1)
+    return x, (nv.w4a16_prepare(dev(W1), dev(SW1)), g1), (nv.w4a16_prepare(dev(W2), dev(SW2)), g2)
+
+
+@pytest.mark.parametrize("M", [1, 20, 144])
+def test_linear_chain_waits_for_the_previous_call(M):
+    # Each call may start before the previous kernel in the stream has finished
+    # (programmatic dependent launch) and must wait for it before reading x: the
+    # second layer reads the first layer's output.  Back-to-back calls must give
+    # the same bits as calls separated by a device synchronisation, every time.
+    x, (w1, g1), (w2, g2) = _chain_inputs(M, 31)
+    y1 = torch.empty((M, 1024), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty((M, 5120), dtype=torch.bfloat16, device="cuda")
+    nv.w4a16_linear(x, w1, g1, 1024, out=y1)
+    torch.cuda.synchronize()
+    nv.w4a16_linear(y1, w2, g2, 5120, out=y2)
+    torch.cuda.synchronize()
+    want1, want2 = y1.clone(), y2.clone()
+    for _ in range(20):
+        y1.zero_()
+        y2.zero_()
+        nv.w4a16_linear(x, w1, g1, 1024, out=y1)
+        nv.w4a16_linear(y1, w2, g2, 5120, out=y2)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert torch.equal(y1.view(torch.int16), want1.view(torch.int16))
+    assert torch.equal(y2.view(torch.int16), want2.view(torch.int16))
+
+
+def test_linear_back_to_back_writes_keep_the_last():
+    # Two calls writing the same y: the result is the second call's.
+    N, K = 5120, 5120
+    W, SW, g = quantized_weight(N, K, 4)
+    wp = nv.w4a16_prepare(dev(W), dev(SW))
+    xa = dev_bf16(G.bf16_normal(1, K, 5, "xa"))
+    xb = dev_bf16(G.bf16_normal(1, K, 6, "xb"))
+    want = nv.w4a16_linear(xb, wp, g, N)
+    torch.cuda.synchronize()
+    y = torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(20):
+        nv.w4a16_linear(xa, wp, g, N, out=y)
+        nv.w4a16_linear(xb, wp, g, N, out=y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), want.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [1, 144])
+def test_linear_graph_replay_matches_eager(M):
+    # The calls allocate nothing and keep no per-call device state, so a captured
+    # chain replays to the same bits as eager execution.
+    x, (w1, g1), (w2, g2) = _chain_inputs(M, 41)
+    e1 = nv.w4a16_linear(x, w1, g1, 1024)
+    e2 = nv.w4a16_linear(e1, w2, g2, 5120)
+    torch.cuda.synchronize()
+    y1 = torch.empty_like(e1)
+    y2 = torch.empty_like(e2)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            nv.w4a16_linear(x, w1, g1, 1024, out=y1, stream=s)
+            nv.w4a16_linear(y1, w2, g2, 5120, out=y2, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        y1.zero_()
+        y2.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert torch.equal(y1.view(torch.int16), e1.view(torch.int16))
+    assert torch.equal(y2.view(torch.int16), e2.view(torch.int16))
