@@ -46,10 +46,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the sub-measurements")
-    ap.add_argument("--only", choices=["w4a16", "producers"], default=None,
+    ap.add_argument("--only", choices=["w4a16", "producers", "llm"], default=None,
                     help="run one sub-measurement alone and print its JSON (for profiling runs)")
     ap.add_argument("--w4a16-shapes", default=None,
                     help="with --only w4a16: comma-separated NxKxM list, e.g. 17408x5120x1")
+    ap.add_argument("--llm-configs", default="0",
+                    help="with --only llm: comma-separated GEMM configs to time (0 = automatic choice)")
     return ap.parse_args()
 
 
@@ -341,6 +343,88 @@ def bench_w4a16(peaks, shapes=None):
     return out
 
 
+LLM_M = (128, 1024, 8192)
+LLM_NK = [(5120, 5120), (17408, 5120), (5120, 17408), (6144, 5120)]
+
+
+def bench_llm(peaks, configs=(0,), shapes=None):
+    """W4A4 GEMM on the LLM linear-layer shapes: activations N(0,1) and weights
+    N(0,0.02) in BF16 (seeded device RNG), quantised by nvfp4_quantize with per-tensor
+    scales, scales packed.  Per-call time from CUDA-graph replay of one call per
+    rotated weight copy (copies totalling >= 4x L2, so each call reads its weight
+    from HBM).  Each cell reports its roofline bound: max(2MNK / FP4 peak, bytes /
+    HBM bandwidth)."""
+    import math
+
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+
+    peak_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    gen = torch.Generator(device="cuda")
+    out = {}
+    if shapes is None:
+        shapes = [(M, N, K) for M in LLM_M for (N, K) in LLM_NK]
+    for (M, N, K) in shapes:
+        gen.manual_seed(M * 7 + N * 3 + K)
+        x = torch.randn((M, K), device="cuda", generator=gen).to(torch.bfloat16)
+        w = (0.02 * torch.randn((N, K), device="cuda", generator=gen)).to(torch.bfloat16)
+        gx = float(x.abs().max().float() / (6 * 448))
+        gw = float(w.abs().max().float() / (6 * 448))
+        A, SFA = nv.quantize(x, gx)
+        B, SFB = nv.quantize(w, gw)
+        del x, w
+        sfa, sfb = nv.pack_scales(SFA, K), nv.pack_scales(SFB, K)
+        wbytes = B.numel() + sfb.numel()
+        copies = min(64, max(2, math.ceil(4 * l2 / wbytes)))
+        Bs = [B] + [B.clone() for _ in range(copies - 1)]
+        sfbs = [sfb] + [sfb.clone() for _ in range(copies - 1)]
+        D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        alpha = gx * gw
+        flops = 2.0 * M * N * K
+        nbytes = M * K // 2 + N * K // 2 + (M + N) * K // 16 + 2 * M * N
+        t_tensor = flops / (peak_fp4 * 1e12) * 1e6
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+        cell = {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                "roofline_us": round(max(t_tensor, t_hbm), 2), "copies": copies}
+        for cfg in configs:
+            for i in range(2):
+                nv.gemm(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, out=D, config=cfg)
+            torch.cuda.synchronize()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for i in range(copies):
+                        nv.gemm(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, out=D, config=cfg, stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+            g.replay()
+            torch.cuda.synchronize()
+            best = None
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / copies
+                best = us if best is None else min(best, us)
+            del g
+            key = "auto" if cfg == 0 else f"config{cfg}"
+            cell[key] = {"us": round(best, 2), "tflops": round(flops / best / 1e6, 1),
+                         "roofline_frac": round(max(t_tensor, t_hbm) / best, 3)}
+        if 0 in configs:
+            cell["auto_config"] = nv.gemm_config_name(nv.gemm_choose_config(M, N, K)).split(" ")[0]
+        out[f"M{M}_N{N}_K{K}"] = cell
+        del A, B, SFA, SFB, sfa, sfb, D, Bs, sfbs
+    err = nv.device_error()
+    if err != 0:
+        raise RuntimeError(f"device error {err}")
+    return out
+
+
 def bench_producers(peaks):
     """quantize and pack_scales at 8192 x 5120: per-call time from CUDA-graph replay of
     one call per rotated input/output copy (copies totalling >= 4x L2, so every call
@@ -475,6 +559,7 @@ def run_ours(args):
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                            "ms_per_step": round(ms, 3)}
             line["w4a16"] = bench_w4a16(peaks)
+            line["llm_w4a4"] = bench_llm(peaks)
             line["producers"] = bench_producers(peaks)
             line["cpu_baseline"] = cpu_baseline_gemm(S)
     if rank == 0:
@@ -549,6 +634,8 @@ def run_only(args):
                 N, K, M = (int(v) for v in item.lower().split("x"))
                 shapes.append((N, K, (M,)))
         out = bench_w4a16(peaks, shapes)
+    elif args.only == "llm":
+        out = bench_llm(peaks, tuple(int(c) for c in args.llm_configs.split(",")))
     else:
         out = bench_producers(peaks)
     print(json.dumps({"only": args.only, "results": out}), flush=True)

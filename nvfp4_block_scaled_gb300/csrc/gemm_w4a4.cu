@@ -81,6 +81,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// A copies held back until the previous grid in the stream has completed (the
+// producers' side of programmatic dependent launch): up to N stages whose B
+// copies are already in flight.  flush() waits for the grid dependency, then
+// issues the held-back copies through load(stage, kb, m_block, n_atoms).
+template <int N>
+struct DeferredA {
+  int n = 0;
+  bool done = false;
+  int st[N], kb[N], mb[N], nk[N];
+  __device__ bool full() const { return !done && n == N; }
+  __device__ void add(int s, int k, int m, int a) {
+    st[n] = s; kb[n] = k; mb[n] = m; nk[n] = a;
+    ++n;
+  }
+  template <typename F>
+  __device__ void flush(F&& load) {
+    griddep_wait();
+    for (int i = 0; i < n; ++i) load(st[i], kb[i], mb[i], nk[i]);
+    done = true;
+  }
+};
+
 template <int BN, int STAGES, int ACC_BUFS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -123,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
 
   const int num_tiles = tiles_m * tiles_n;
   const int KB = (K + kBK - 1) / kBK;
@@ -136,6 +159,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
+      // The first STAGES stages' B (weight) copies go out before waiting for the
+      // previous grid in the stream (programmatic launch); their A copies, which
+      // that grid may produce, are deferred until after the wait.
+      DeferredA<STAGES> dfr;
+      auto load_a = [&](int st, int kb, int mb, int nk) {
+        const uint32_t fb = bar_full + 8 * st;
+        tma_load_2d(sbase + C::kOffA + st * C::kABytes, &tmA, fb, kb * kBKBytes, mb * kBM, pol);
+        bulk_load(sbase + C::kOffSFA + st * C::kSFABytes, SFA + (static_cast<size_t>(mb) * KG + kb * kKSteps) * kAtom,
+                  nk * kAtom, fb, pol);
+      };
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, tiles_m, tiles_n, group_n, mb, nb);
@@ -144,24 +177,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < C::kBands; ++b) nbv += (nb * C::kBands + b < bands_n) ? 1 : 0;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
+          if (dfr.full()) dfr.flush(load_a);
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           const int nk = min(kKSteps, KG - kb * kKSteps);
           const uint32_t bytes = C::kABytes + C::kBBytes + nk * kAtom * (1 + nbv);
           const uint32_t fb = bar_full + 8 * stage;
           mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sbase + C::kOffA + stage * C::kABytes, &tmA, fb, kb * kBKBytes, mb * kBM, pol);
           tma_load_2d(sbase + C::kOffB + stage * C::kBBytes, &tmB, fb, kb * kBKBytes, nb * BN, pol);
-          bulk_load(sbase + C::kOffSFA + stage * C::kSFABytes,
-                    SFA + (static_cast<size_t>(mb) * KG + kb * kKSteps) * kAtom, nk * kAtom, fb, pol);
           for (int b = 0; b < nbv; ++b)
             bulk_load(sbase + C::kOffSFB + stage * C::kSFBBytes + b * kKSteps * kAtom,
                       SFB + (static_cast<size_t>(nb * C::kBands + b) * KG + kb * kKSteps) * kAtom,
                       nk * kAtom, fb, pol);
+          if (dfr.done) load_a(stage, kb, mb, nk); else dfr.add(stage, kb, mb, nk);
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
       }
+      if (!dfr.done) dfr.flush(load_a);
       // After an abort, wait (briefly, bounded) for the copies still in flight
       // before the thread block releases its shared memory.
       if (*abort_flag) {
@@ -175,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      griddep_wait();  // time-limited waits start once the previous grid is done
       constexpr uint32_t idesc = idesc_nvf4_m128<BN>();
       int stage = 0;
       uint32_t phase = 0;
@@ -218,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
+    griddep_wait();
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -260,6 +295,272 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ split-K kernel
+//
+// For shapes whose output tiles cannot fill the SMs (few tokens: M = 128 against
+// 5120..17408 weight rows gives 20..68 tiles of 128 x 256 for 152 SMs), K is split
+// over a thread block cluster of S CTAs (S <= 8).  Every CTA of the cluster computes
+// the same 128 x BN tile over a contiguous range of the K blocks, with the
+// producer / MMA / epilogue roles of gemm_nvf4_kernel.  Its epilogue warps park the
+// FP32 partial tile in the CTA's own shared memory (the drained operand ring), and
+// after a cluster barrier CTA r finalises rows [128 r / S, 128 (r + 1) / S) of the
+// tile: it reads the S partials through distributed shared memory, adds them in
+// rank order (a fixed order: repeated calls are bit-identical), multiplies by alpha
+// and stores BF16.  No global workspace is involved.
+//
+// Partial-tile layout: row r (TMEM lane) holds BN floats as BN/4 16-byte chunks;
+// chunk c sits at position c ^ (r % 8), so the eight rows written by one phase of a
+// warp's 16-byte stores fall in different banks.
+// Twelve warps: producer, MMA issuer, then ten more that wait for the accumulator.
+// Eight of them (two per TMEM lane quarter) push the partial tile; all twelve sum the
+// owned columns.  The extra warps are there for latency hiding in those two phases,
+// which are short dependent chains per warp.
+constexpr int kSplitThreads = 384;
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kSplitThreads, 1)
+    gemm_nvf4_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const uint8_t* __restrict__ SFA, const uint8_t* __restrict__ SFB,
+                            __nv_bfloat16* __restrict__ D, float alpha, int M, int N, int K, int S) {
+  using C = Cfg<BN, STAGES, 1>;
+  // The receive slots (at most S x 128 rows x (ceil(BN/8 / S) x 32 + 16) bytes, largest
+  // for S = 6 or 7) fit in the drained operand ring, below the per-unit table at its end.
+  static_assert(6 * 128 * (((BN / 8 + 5) / 6) * 32 + 16) + 8 * (BN / 8) <= C::kOffBar &&
+                    7 * 128 * (((BN / 8 + 6) / 7) * 32 + 16) + 8 * (BN / 8) <= C::kOffBar &&
+                    8 * 128 * (((BN / 8 + 7) / 8) * 32 + 16) + 8 * (BN / 8) <= C::kOffBar &&
+                    5 * 128 * (((BN / 8 + 4) / 5) * 32 + 16) + 8 * (BN / 8) <= C::kOffBar,
+                "partial-sum slots fit in the operand ring");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + C::kOffBar;
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_accf = bar_empty + 8 * STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = blockIdx.x;  // the cluster spans gridDim.x == S CTAs: rank == blockIdx.x
+  const int nb = blockIdx.y;
+  const int mb = blockIdx.z;
+  const int KB = (K + kBK - 1) / kBK;
+  const int kb0 = rank * KB / S, kb1 = (rank + 1) * KB / S;
+  const int KG = K / kMmaK;
+  const int bands_n = (N + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_accf, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      int nbv = 0;
+#pragma unroll
+      for (int b = 0; b < C::kBands; ++b) nbv += (nb * C::kBands + b < bands_n) ? 1 : 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      DeferredA<STAGES> dfr;  // B first, A after the grid dependency (see gemm_nvf4_kernel)
+      auto load_a = [&](int st, int kb, int m, int nk) {
+        const uint32_t fb = bar_full + 8 * st;
+        tma_load_2d(sbase + C::kOffA + st * C::kABytes, &tmA, fb, kb * kBKBytes, m * kBM, pol);
+        bulk_load(sbase + C::kOffSFA + st * C::kSFABytes, SFA + (static_cast<size_t>(m) * KG + kb * kKSteps) * kAtom,
+                  nk * kAtom, fb, pol);
+      };
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (dfr.full()) dfr.flush(load_a);
+        if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) break;
+        const int nk = min(kKSteps, KG - kb * kKSteps);
+        const uint32_t fb = bar_full + 8 * stage;
+        mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes + nk * kAtom * (1 + nbv));
+        tma_load_2d(sbase + C::kOffB + stage * C::kBBytes, &tmB, fb, kb * kBKBytes, nb * BN, pol);
+        for (int b = 0; b < nbv; ++b)
+          bulk_load(sbase + C::kOffSFB + stage * C::kSFBBytes + b * kKSteps * kAtom,
+                    SFB + (static_cast<size_t>(nb * C::kBands + b) * KG + kb * kKSteps) * kAtom, nk * kAtom, fb,
+                    pol);
+        if (dfr.done) load_a(stage, kb, mb, nk); else dfr.add(stage, kb, mb, nk);
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!dfr.done) dfr.flush(load_a);
+      if (*abort_flag) {
+        for (int i = 0; i < STAGES && issued > 0; ++i) {
+          --issued;
+          if (--stage < 0) { stage = STAGES - 1; phase ^= 1; }
+          mbar_wait_for(bar_full + 8 * stage, phase, 10000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      griddep_wait();
+      constexpr uint32_t idesc = idesc_nvf4_m128<BN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) break;
+        tc_fence_after();
+        const int nk = min(kKSteps, KG - kb * kKSteps);
+        const uint32_t sfa_t = tmem + C::kTmemSF + stage * (C::kSFACols + C::kSFBCols);
+        const uint32_t sfb_t = sfa_t + C::kSFACols;
+        const uint32_t sA = sbase + C::kOffA + stage * C::kABytes;
+        const uint32_t sB = sbase + C::kOffB + stage * C::kBBytes;
+        const uint32_t sSFA = sbase + C::kOffSFA + stage * C::kSFABytes;
+        const uint32_t sSFB = sbase + C::kOffSFB + stage * C::kSFBBytes;
+        for (int j = 0; j < nk; ++j) {
+          tc_cp_32x128b_warpx4(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+#pragma unroll
+          for (int b = 0; b < C::kBands; ++b)
+            tc_cp_32x128b_warpx4(sfb_t + 4 * (j * C::kBands + b),
+                                 make_sdesc(sSFB + (b * kKSteps + j) * kAtom, 0, 128, 0));
+        }
+        for (int j = 0; j < nk; ++j) {
+          const uint64_t adesc = make_sdesc(sA + j * (kMmaK / 2), 16, 1024, 2);
+          const uint64_t bdesc = make_sdesc(sB + j * (kMmaK / 2), 16, 1024, 2);
+          tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * j * C::kBands,
+                      (kb != kb0 || j != 0) ? 1u : 0u);
+        }
+        tc_commit(bar_empty + 8 * stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      tc_commit(bar_accf);  // also when the loop gave up: lets the epilogue proceed
+    }
+  } else {
+    griddep_wait();
+    warp_wait(bar_accf, 0, abort_flag);  // (gives up only together with the other roles)
+  }
+
+  // ------------------------------------------------------------ push the partial tile to its owners
+  // The tile's columns form nu = BN/8 units of 8; CTA k owns units [k nu / S, (k+1) nu / S).
+  // Owner k receives, in its ring, one slot per source rank: 128 rows x (its units x 8)
+  // FP32, rows padded by 16 bytes (so the eight rows written by one phase of 16-byte
+  // stores fall in different banks).  The stores are posted (no round trip).  A small
+  // table (per unit: the shared::cluster address of row 0 of this CTA's slot at the
+  // owner, and the owner's row pitch) is filled first, so the push loop itself does
+  // no division.
+  constexpr int kNu = BN / 8;
+
+  // Every CTA's accumulator is complete (and its operand ring drained) past this
+  // barrier, so the rings can receive the partial sums (and hold the table).
+  tc_fence_before();
+  __syncwarp();
+  griddep_wait();  // D may still be written by the previous grid in the stream
+  cluster_sync_all();
+  tc_fence_after();
+
+  uint32_t* unit_tab = reinterpret_cast<uint32_t*>(smem + C::kOffBar - 2 * 4 * kNu);
+  if (threadIdx.x < kNu) {
+    const int u = threadIdx.x;
+    const int k = ((u + 1) * S - 1) / kNu;  // owner of unit u
+    const int u0 = k * kNu / S, uk = (k + 1) * kNu / S - u0;
+    const uint32_t pitch = static_cast<uint32_t>(uk * 32 + 16);
+    const uint32_t off = static_cast<uint32_t>(rank) * 128u * pitch + static_cast<uint32_t>(u - u0) * 32u;
+    unit_tab[2 * u] = map_to_rank(sbase + off, static_cast<uint32_t>(k));
+    unit_tab[2 * u + 1] = pitch;
+  }
+  __syncthreads();
+
+  if (warp >= 2 && warp < 10) {
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int half = (warp - 2) >> 2;       // which half of the columns
+    const uint32_t r = static_cast<uint32_t>(q * 32 + lane);
+    const uint32_t t_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+      uint32_t v[32];
+      tc_ld_32x32b_x32(t_base + c * 32, v);
+      tc_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t dst = unit_tab[2 * (4 * c + i)] + r * unit_tab[2 * (4 * c + i) + 1];
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[8 * i]),
+                     "r"(v[8 * i + 1]), "r"(v[8 * i + 2]), "r"(v[8 * i + 3])
+                     : "memory");
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16), "r"(v[8 * i + 4]),
+                     "r"(v[8 * i + 5]), "r"(v[8 * i + 6]), "r"(v[8 * i + 7])
+                     : "memory");
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();  // every partial has landed at its owner
+
+  // ------------------------------------------------------------ fixed-order sum of the owned columns
+  // Item = one row x one 8-column unit (two 16-byte chunks per slot, one 16-byte
+  // BF16 store); each thread takes two items at a time so their loads overlap.
+  {
+    const int u0 = rank * kNu / S, uk = (rank + 1) * kNu / S - u0;
+    const uint32_t pitch = static_cast<uint32_t>(uk * 32 + 16);
+    const uint32_t slot = 128u * pitch;
+    const int items = 128 * uk;
+    const int gcol0 = nb * BN + u0 * 8;
+    for (int base = threadIdx.x; base < items; base += 2 * kSplitThreads) {
+      float a[2][8];
+      int row[2], un[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int idx = base + h * kSplitThreads;
+        row[h] = idx / uk;  // uk is small; one division per item
+        un[h] = idx - row[h] * uk;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[h][e] = 0.f;
+        if (idx < items) {
+          const uint32_t off = sbase + static_cast<uint32_t>(row[h]) * pitch + static_cast<uint32_t>(un[h]) * 32u;
+#pragma unroll 1
+          for (int s = 0; s < S; ++s) {
+            float4 lo, hi;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w)
+                         : "r"(off + static_cast<uint32_t>(s) * slot));
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
+                         : "r"(off + static_cast<uint32_t>(s) * slot + 16u));
+            a[h][0] += lo.x; a[h][1] += lo.y; a[h][2] += lo.z; a[h][3] += lo.w;
+            a[h][4] += hi.x; a[h][5] += hi.y; a[h][6] += hi.z; a[h][7] += hi.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int idx = base + h * kSplitThreads;
+        const int grow = mb * kBM + row[h];
+        const int gcol = gcol0 + un[h] * 8;
+        if (idx < items && grow < M && gcol < N)
+          *reinterpret_cast<uint4*>(D + static_cast<size_t>(grow) * N + gcol) =
+              make_uint4(pack_bf16x2(alpha * a[h][0], alpha * a[h][1]), pack_bf16x2(alpha * a[h][2], alpha * a[h][3]),
+                         pack_bf16x2(alpha * a[h][4], alpha * a[h][5]), pack_bf16x2(alpha * a[h][6], alpha * a[h][7]));
+      }
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
 
 // ------------------------------------------------------------------ CTA-pair kernel
 //
@@ -365,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
 
   const int num_tiles = tiles_m * tiles_n;
   const int KB = (K + kBKP - 1) / kBKP;
@@ -377,23 +679,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // B first, A after the grid dependency (see gemm_nvf4_kernel).
+      DeferredA<kStages> dfr;
+      auto load_a = [&](int st, int kb, int mt, int) {
+        const uint32_t fb = full_leader + 8 * st;
+        tma_load_3d_pair(sbase + kOffA + st * kABytes, &tmA, fb, 0, mt * 256 + static_cast<int>(rank) * 128,
+                         (kBKP / 256) * kb);
+        tma_load_3d_pair(sbase + kOffSFA + st * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
+                         mt * 2 + static_cast<int>(rank));
+      };
       for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
         int mt, nt;
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
-        const int a_row = mt * 256 + static_cast<int>(rank) * 128;
         const int b_row = nt * 256 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < KB; ++kb) {
+          if (dfr.full()) dfr.flush(load_a);
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
           const uint32_t fb = full_leader + 8 * stage;
-          tma_load_3d_pair(sbase + kOffA + stage * kABytes, &tmA, fb, 0, a_row, (kBKP / 256) * kb);
           tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * kb);
-          tma_load_3d_pair(sbase + kOffSFA + stage * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
-                           mt * 2 + static_cast<int>(rank));
           tma_load_3d_pair(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, kb * kStepsP, nt * 2);
+          if (dfr.done) load_a(stage, kb, mt, 0); else dfr.add(stage, kb, mt, 0);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
+      if (!dfr.done) dfr.flush(load_a);
       // Drain: wait until every stage has been released once more, so that no commit
       // arrival (and no copy of this CTA) is still in flight when the CTA exits.
       for (int i = 0; i < kStages && !*abort_flag; ++i) {
@@ -407,6 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (leader && lane == 0) {
+      griddep_wait();  // time-limited waits start once the previous grid is done
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -445,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stage only refills (and its full barrier only completes) after the MMAs that
     // read the slot have committed.
     if (leader && lane == 0) {
+      griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -469,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (8 warps, both CTAs)
+    griddep_wait();
     const int q = warp & 3;                        // TMEM lane quarter of this warp
     const int h = (warp - kFirstEpiWarp) >> 2;     // column half (0: columns 0..127, 1: 128..255)
     const uint32_t acce_leader = map_to_rank(bar_acce, 0);
@@ -545,8 +858,18 @@ constexpr ConfigEntry kConfigs[] = {
     {"1cta_128x256_s3_acc1", 256},
     {"1cta_128x128_s4_acc2", 128},
     {"2cta_256x256_k256x4 (K % 256 == 0; other K run 1cta_128x256)", 256},
+    {"1cta_128x256_splitk (K split over a cluster of up to 8 CTAs, fixed-order DSMEM reduction)", 256},
+    {"1cta_128x128_splitk (K split over a cluster of up to 8 CTAs, fixed-order DSMEM reduction)", 128},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
+
+// Programmatic dependent launch: the kernel may start while the previous kernel in
+// the stream finishes; it streams its first weight stages and waits
+// (griddepcontrol.wait) before it reads A or writes D.
+inline void set_programmatic(cudaLaunchAttribute& a) {
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+}
 
 template <int BN, int STAGES, int ACC_BUFS>
 nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
@@ -569,10 +892,92 @@ nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const u
   const int num_tiles = tiles_m * tiles_n;
   const int grid = num_tiles < dev.num_sms ? num_tiles : dev.num_sms;
   const int group_n = tiles_n < 8 ? tiles_n : 8;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(ta, tb, SFA, SFB, static_cast<__nv_bfloat16*>(D), alpha,
-                                                   static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                                                   tiles_m, tiles_n, group_n);
-  return from_cuda(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  set_programmatic(attr[0]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, SFA, SFB, static_cast<__nv_bfloat16*>(D), alpha,
+                                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), tiles_m, tiles_n,
+                                      group_n));
+}
+
+// K split for a shape.  Clusters of S CTAs (one CTA per SM) must fit inside a GPC,
+// so how many run at once is queried per S (cudaOccupancyMaxActiveClusters) rather
+// than derived from the SM count.  The cost model: waves x (K blocks per CTA + 2),
+// the 2 standing for the partial-sum exchange; S <= 8 (a portable cluster) and at
+// least two K = 256 blocks per CTA when K allows.
+int splitk_factor(int64_t tiles, int64_t K, const int (&active)[9]) {
+  const int64_t KB = (K + kBK - 1) / kBK;
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int S = 1; S <= 8; ++S) {
+    if (S > 1 && S > KB / 2) break;
+    const int64_t act = active[S] > 0 ? active[S] : 1;
+    const int64_t waves = (tiles + act - 1) / act;
+    const int64_t cost = waves * ((KB + S - 1) / S + 2);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = S; }
+  }
+  return best;
+}
+
+template <int BN, int STAGES>
+nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
+                        void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+  using C = Cfg<BN, STAGES, 1>;
+  auto kern = gemm_nvf4_splitk_kernel<BN, STAGES>;
+  static bool attr_set[64] = {};
+  static int active[64][9] = {};  // co-resident clusters of S CTAs, per device
+  const int d = dev.device < 64 ? dev.device : 63;
+  if (!attr_set[d]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    for (int s = 1; s <= 8; ++s) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(s, 1, 1);
+      qc.blockDim = dim3(kSplitThreads, 1, 1);
+      qc.dynamicSmemBytes = C::kSmemBytes;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = s;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess) n = 0;
+      active[d][s] = n > 0 ? n : dev.num_sms / s;
+    }
+    attr_set[d] = true;
+  }
+  const int64_t tiles_m = (M + kBM - 1) / kBM;
+  const int64_t tiles_n = (N + BN - 1) / BN;
+  if (tiles_m > 65535 || tiles_n > 65535) return run<BN, STAGES, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+  const int S = splitk_factor(tiles_m * tiles_n, K, active[d]);
+  CUtensorMap ta, tb;
+  nvfp4_status st = encode_tmap_u8_2d(&ta, A, K / 2, M, K / 2, kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != NVFP4_OK) return st;
+  st = encode_tmap_u8_2d(&tb, B, K / 2, N, K / 2, kBKBytes, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != NVFP4_OK) return st;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m));
+  cfg.blockDim = dim3(kSplitThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  set_programmatic(attr[1]);
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, SFA, SFB, static_cast<__nv_bfloat16*>(D), alpha,
+                                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), S));
 }
 
 nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
@@ -621,13 +1026,14 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   cfg.blockDim = dim3(pair::kThreads, 1, 1);
   cfg.dynamicSmemBytes = pair::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  set_programmatic(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, tsfa, tsfb, td, alpha, static_cast<int>(K), tiles_m,
                                       tiles_n, group_n));
 }
@@ -652,11 +1058,18 @@ const char* gemm_config_name(int config) {
 }
 
 int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-  // CTA pairs (256 x 256 tiles, four K = 256 stages) whenever the tile is filled in both
-  // dimensions and K allows the 3-D operand boxes; 128 x 256 single-CTA tiles for
-  // skinny M; 128 x 128 when N is narrow or the problem is too small to fill the SMs.
-  if (K % 256 == 0 && M > 128 && N > 128) return 3;
+  // Few output tiles (at most half the SMs busy with 128 x 256 tiles) and at least
+  // two K = 256 blocks: split K over a cluster.  Otherwise CTA pairs (256 x 256
+  // tiles, four K = 256 stages) whenever the tile is filled in both dimensions and K
+  // allows the 3-D operand boxes; 128 x 256 single-CTA tiles for skinny M; 128 x 128
+  // when N is narrow.
   const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+  const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
+  // Split K over 128 x 128 tiles unless those alone nearly fill the SMs (then over
+  // 128 x 256 tiles, whose smaller split moves fewer partial sums): measured on the
+  // 128-token layer shapes, e.g. 11.8 us against 17.4 us at N = K = 5120.
+  if (2 * tiles256 <= dev.num_sms && K >= 512) return (5 * tiles128 >= 4 * dev.num_sms && N > 128) ? 4 : 5;
+  if (K % 256 == 0 && M > 128 && N > 128) return 3;
   if (N <= 128 || tiles256 < dev.num_sms / 2) return 2;
   return 1;
 }
@@ -670,6 +1083,8 @@ nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const
     case 3:
       if (K % 256 != 0) return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
       return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+    case 4: return run_splitk<256, 3>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+    case 5: return run_splitk<128, 4>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
     default: return NVFP4_ERR_INVALID_ARG;
   }
 }

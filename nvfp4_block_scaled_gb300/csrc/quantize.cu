@@ -42,6 +42,8 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
 __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t nblocks,
                                                        float g, uint2* __restrict__ codes,
                                                        uint8_t* __restrict__ sf) {
+  griddep_wait();                // x may be produced by the previous grid in the stream
+  griddep_launch_dependents();   // a following GEMM may start streaming its weights
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
     const uint4 v0 = __ldcs(x + 2 * b);
@@ -92,6 +94,8 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restr
                                                           int64_t num_tiles, bool word_loads,
                                                           uint32_t* __restrict__ out) {
   __shared__ uint32_t tile[128 * kPackPitch];
+  griddep_wait();
+  griddep_launch_dependents();
   for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
     const int64_t band = t / tiles_per_band;
     const int64_t g0 = (t - band * tiles_per_band) * kPackAtoms;
@@ -137,6 +141,24 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restr
   }
 }
 
+// Launch configuration with programmatic dependent launch allowed (the kernels wait
+// for the previous grid in the stream before touching memory).
+cudaLaunchConfig_t programmatic_config(int grid, int threads, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  return cfg;
+}
+
+void set_programmatic(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1]) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
 int grid_for(int64_t work_items, int threads, const DeviceInfo& dev, int per_sm) {
   const int64_t need = (work_items + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * per_sm;
@@ -149,9 +171,11 @@ nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, ui
                              cudaStream_t stream, const DeviceInfo& dev) {
   const int64_t nblocks = rows * (K / 16);
   const int grid = grid_for(nblocks, 256, dev, 8);
-  quantize_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), nblocks, g,
-                                            reinterpret_cast<uint2*>(codes), sf);
-  return from_cuda(cudaGetLastError());
+  cudaLaunchConfig_t cfg = programmatic_config(grid, 256, stream);
+  cudaLaunchAttribute attr[1];
+  set_programmatic(cfg, attr);
+  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_kernel, static_cast<const uint4*>(x), nblocks, g,
+                                      reinterpret_cast<uint2*>(codes), sf));
 }
 
 nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out, cudaStream_t stream,
@@ -163,9 +187,11 @@ nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint
   const int64_t tiles_per_band = (groups + kPackAtoms - 1) / kPackAtoms;
   const int64_t num_tiles = bands * tiles_per_band;
   const int grid = grid_for(num_tiles * 256, 256, dev, 8);
-  pack_scales_kernel<<<grid, 256, 0, stream>>>(sf, rows, C, groups, tiles_per_band, num_tiles, word_loads,
-                                               reinterpret_cast<uint32_t*>(out));
-  return from_cuda(cudaGetLastError());
+  cudaLaunchConfig_t cfg = programmatic_config(grid, 256, stream);
+  cudaLaunchAttribute attr[1];
+  set_programmatic(cfg, attr);
+  return from_cuda(cudaLaunchKernelEx(&cfg, pack_scales_kernel, sf, rows, C, groups, tiles_per_band, num_tiles,
+                                      word_loads, reinterpret_cast<uint32_t*>(out)));
 }
 
 }  // namespace nvfp4

@@ -128,16 +128,6 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
   return v;
 }
 
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t local_addr, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote));
-  return v;
-}
-
 // Dequantise one word (8 codes) into the 4 A-fragment registers, times the
 // row scales (s_lo for rows g, s_hi for rows g+8, both bf16x2 {s, s}).
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_lo, uint32_t s_hi, uint32_t (&a)[4]) {

@@ -141,6 +141,20 @@ def test_gemm_large_square_zero_and_subnormal_scales(S):
     check_sampled(A, SFA, B, SFB, alpha, D, S, S, 1024, f"{S}^3 zero/subnormal scales")
 
 
+@pytest.mark.parametrize("config", [4, 5])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 4096), (200, 136, 2048), (128, 520, 1344), (384, 264, 17408)])
+def test_gemm_split_k_over_a_cluster(config, M, N, K):
+    # Few tiles and long K: the K blocks are split over clusters of 2..8 CTAs
+    # (uneven ranges when the block count is not a multiple; a ragged last block
+    # when K % 256 != 0) and reduced in rank order through distributed shared memory.
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=K + N, scales="zero_sub")
+    alpha = G.alpha_uniform(K)
+    D = run_gemm(A, SFA, B, SFB, alpha, M, N, K, config)
+    check_full(A, SFA, B, SFB, alpha, D, f"split-K {M}x{N}x{K} config {config}")
+    D2 = run_gemm(A, SFA, B, SFB, alpha, M, N, K, config)
+    assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+
+
 def test_gemm_repeat_is_bit_identical():
     M, N, K = 1024, 1024, 2048
     A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=5)
@@ -173,3 +187,70 @@ def test_gemm_llm_linear(M, N, K):
         check_full(Ah, SFAh, Bh, SFBh, alpha, D, f"llm {M}x{N}x{K}")
     else:
         check_sampled(Ah, SFAh, Bh, SFBh, alpha, D, M, N, 1024, f"llm {M}x{N}x{K}")
+
+
+def _llm_operands(M, N, K, seed):
+    x = G.bf16_normal(M, K, seed, "x")
+    w = G.bf16_normal(N, K, seed, "w", 0.02)
+    return dev_bf16(x), dev_bf16(w), O.global_scale(x), O.global_scale(w)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 5120, 5120), (512, 1024, 2048), (96, 768, 1024)])
+def test_quantize_pack_gemm_chain_back_to_back(M, N, K):
+    # quantize -> pack -> GEMM -> W4A16 (reading D as its activations), issued
+    # back to back: every kernel may start before its predecessor ends (programmatic
+    # launch) and must wait for it before reading what it wrote.  The chain must give
+    # the bits of the same calls separated by device synchronisations, every time.
+    x, w, gx, gw = _llm_operands(M, N, K, 17)
+    B, SFB = nv.quantize(w, gw)
+    sfb = nv.pack_scales(SFB, K)
+    W2 = G.packed_codes_uniform(256, N, 3, "W2")
+    S2 = G.scales_uniform_normal(256, N, 3, "S2")
+    wp2 = nv.w4a16_prepare(dev(W2), dev(S2))
+    A = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    SFA = torch.empty((M, K // 16), dtype=torch.uint8, device="cuda")
+    sfa = torch.empty(nv.packed_scales_bytes(M, K), dtype=torch.uint8, device="cuda")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((M, 256), dtype=torch.bfloat16, device="cuda")
+    alpha = float(np.float32(gx) * np.float32(gw))
+
+    def chain(sync):
+        s = torch.cuda.synchronize if sync else (lambda: None)
+        nv.quantize(x, gx, A, SFA)
+        s()
+        nv.pack_scales(SFA, K, sfa)
+        s()
+        nv.gemm(A, sfa, B, sfb, alpha, M, N, K, out=D)
+        s()
+        nv.w4a16_linear(D, wp2, 0.5, 256, out=y)
+        s()
+
+    chain(True)
+    torch.cuda.synchronize()
+    want_d, want_y = D.clone(), y.clone()
+    Ah, SFAh = O.quantize(G.bf16_normal(M, K, 17, "x"), gx)
+    assert np.array_equal(A.cpu().numpy(), Ah) and np.array_equal(SFA.cpu().numpy(), SFAh)
+    for _ in range(10):
+        for t in (A, SFA, sfa, D, y):
+            t.zero_()
+        chain(False)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert torch.equal(D.view(torch.int16), want_d.view(torch.int16))
+    assert torch.equal(y.view(torch.int16), want_y.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 2048, 4096), (1024, 1024, 1024)])
+def test_gemm_back_to_back_writes_keep_the_last(M, N, K):
+    A1, SFA1, B, SFB = G.gemm_square_inputs(M, N, K, seed=6)
+    A2, SFA2, _, _ = G.gemm_square_inputs(M, N, K, seed=7)
+    sfa1, sfa2 = nv.pack_scales(dev(SFA1), K), nv.pack_scales(dev(SFA2), K)
+    a1, a2, b, sfb = dev(A1), dev(A2), dev(B), nv.pack_scales(dev(SFB), K)
+    want = nv.gemm(a2, sfa2, b, sfb, 1.0, M, N, K)
+    torch.cuda.synchronize()
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(10):
+        nv.gemm(a1, sfa1, b, sfb, 1.0, M, N, K, out=D)
+        nv.gemm(a2, sfa2, b, sfb, 1.0, M, N, K, out=D)
+    torch.cuda.synchronize()
+    assert torch.equal(D.view(torch.int16), want.view(torch.int16))
