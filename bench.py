@@ -42,7 +42,7 @@ S_MAIN = 8192
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the sub-measurements")
@@ -52,6 +52,8 @@ def parse():
                     help="with --only w4a16: comma-separated NxKxM list, e.g. 17408x5120x1")
     ap.add_argument("--llm-configs", default="0",
                     help="with --only llm: comma-separated GEMM configs to time (0 = automatic choice)")
+    ap.add_argument("--llm-shapes", default=None,
+                    help="with --only llm: comma-separated MxNxK list (default: every LLM layer shape)")
     return ap.parse_args()
 
 
@@ -117,12 +119,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "10"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # nvidia-smi needs a moment to start: wait for its first sample so that the
+        # samples cover the timed region that follows
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 3.0:
+            time.sleep(0.005)
+        self.first = len(self.samples)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -131,6 +139,7 @@ class ClockSampler:
                 self.samples.append(parts)
 
     def stop(self):
+        self.last = len(self.samples)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -141,14 +150,17 @@ class ClockSampler:
             self.thread.join(timeout=2)
 
     def summary(self):
-        if not self.samples:
+        """Samples taken between the start and the end of the timed region (the timed
+        launches are asynchronous: the region ends at the synchronisation)."""
+        window = self.samples[getattr(self, "first", 0):getattr(self, "last", len(self.samples))]
+        if not window:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "", 1).isdigit()]
-        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "", 1).isdigit()]
+        sm = [float(s[1]) for s in window if s[1].replace(".", "", 1).isdigit()]
+        mx = [float(s[2]) for s in window if s[2].replace(".", "", 1).isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for s in self.samples for n, v in zip(names, s[5:9]) if v.strip().lower() == "active"})
+        reasons = sorted({n for s in window for n, v in zip(names, s[5:9]) if v.strip().lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(window)}
 
 
 def kernel_source_hash():
@@ -635,7 +647,10 @@ def run_only(args):
                 shapes.append((N, K, (M,)))
         out = bench_w4a16(peaks, shapes)
     elif args.only == "llm":
-        out = bench_llm(peaks, tuple(int(c) for c in args.llm_configs.split(",")))
+        shapes = None
+        if args.llm_shapes:
+            shapes = [tuple(int(v) for v in item.lower().split("x")) for item in args.llm_shapes.split(",")]
+        out = bench_llm(peaks, tuple(int(c) for c in args.llm_configs.split(",")), shapes)
     else:
         out = bench_producers(peaks)
     print(json.dumps({"only": args.only, "results": out}), flush=True)

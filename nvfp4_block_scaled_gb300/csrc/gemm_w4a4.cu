@@ -14,7 +14,11 @@
 //   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator, alpha in FP32,
 //               round-to-nearest-even to BF16, stores to D.
 // Tiles are 128 x BN (BN = 128 or 256) per CTA; a persistent grid walks them in a
-// grouped raster so that a wave shares A rows and B columns in L2.
+// grouped raster so that a wave shares A rows and B columns in L2.  Large shapes run
+// the CTA-pair kernel (256 x 256 tiles); shapes with few tiles split K over a
+// thread block cluster (the split-K kernel).  Every kernel supports programmatic
+// dependent launch: its producer streams the first weight (B) stages before it
+// waits for the previous grid in the stream, and loads A only after.
 
 #include <cuda_bf16.h>
 
