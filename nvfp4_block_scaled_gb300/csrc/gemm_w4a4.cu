@@ -572,20 +572,23 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64 per instruction).  Each CTA
 // stages its own 128 rows of A and its own 128 rows of B.
 //
-// Operand delivery: under load a TMA copy takes about 1.4 us to land, so what
-// bounds the feed is the number of bytes in flight, and shared memory caps that.
-// Four stages of K = 256 keep three stages (about 1.6 us of MMA work) in flight
-// while one is consumed; two stages of K = 512 (the same bytes) covered only one
-// and measured 6-8 % slower at 8192^3 and 16384^3.  Per stage A and B arrive as
-// one 16 KB box each (128 rows x 128 bytes, 128-byte swizzle), the scale atoms as
-// one SFA box (4 atoms, 2 KB) and one SFB box (4 atoms of each of the tile's two
-// bands, 4 KB).  All of both CTAs' copies complete on the leader's "full" barrier.  A scale warp of the leader moves the atoms into the stage's TMEM
-// slot with tcgen05.cp and commits to an "sf" barrier; the leader's MMA thread waits
-// for both, issues the stage's eight MMAs and releases the stage to both CTAs with a
-// multicast commit.  (The copies are the costly part of the tensor pipe's work here:
-// 12 per 4 MMAs; issuing them from their own thread lets them overlap MMA issue.)  Eight epilogue warps per CTA
-// drain the accumulator (128 lanes x 256 columns) into a 128-byte-swizzled BF16
-// staging tile, release the accumulator, and write D with TMA stores.
+// Operand delivery: under load a TMA copy takes about 1.4 us to land, so the
+// feed needs bytes in flight, and shared memory caps them.  Four stages of K = 256
+// keep three stages in flight while one is consumed; two stages of K = 512 (the
+// same bytes) measured 6-8 % slower at 8192^3 and 16384^3, and with four stages
+// loading only half of every B tile saves nothing: the feed no longer bounds the
+// kernel.  Per stage A and B arrive as one 16 KB box each (128 rows x 128 bytes,
+// 128-byte swizzle), the scale atoms as one SFA box (4 atoms, 2 KB) and one SFB box
+// (4 atoms of each of the tile's two bands, 4 KB).  All of both CTAs' copies
+// complete on the leader's "full" barrier.
+//
+// Three scale warps of the leader move the atoms into the stage's TMEM slot with
+// tcgen05.cp (12 copies per 4 MMAs, the costly part of the tensor pipe's work
+// here) and commit to an "sf" barrier; the leader's MMA thread waits for both,
+// issues the stage's four MMAs and releases the stage to both CTAs with a multicast
+// commit.  Eight epilogue warps per CTA drain the accumulator (128 lanes x 256
+// columns) into a 128-byte-swizzled BF16 staging tile, release the accumulator,
+// and write D with TMA stores.
 namespace pair {
 
 constexpr int kStages = 4;
@@ -593,8 +596,9 @@ constexpr int kBKP = 256;                        // K per stage
 constexpr int kStepsP = kBKP / kMmaK;            // 4 MMAs per stage
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2;
-constexpr int kSFWarp = kFirstEpiWarp + kEpiWarps;  // issues the scale copies into TMEM
-constexpr int kThreads = 32 * (kSFWarp + 1);
+constexpr int kSFWarp = kFirstEpiWarp + kEpiWarps;  // first of the warps issuing the scale copies
+constexpr int kSFWarps = 3;                         // one per copy stream: SFA, SFB band 0, SFB band 1
+constexpr int kThreads = 32 * (kSFWarp + kSFWarps);
 constexpr int kABytes = 128 * (kBKP / 2);        // 16 KB: 128 rows x 128 B
 constexpr int kBBytes = 128 * (kBKP / 2);        // 16 KB
 constexpr int kSubTile = 128 * 128;              // 16 KB
@@ -653,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, 2 * kEpiWarps);
-    for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, kSFWarps);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -752,13 +756,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
     }
-  } else if (warp == kSFWarp) {
+  } else if (warp >= kSFWarp) {
     // ------------------------------------------------------------ scale copies (leader CTA)
-    // Moves each landed stage's scale atoms into its TMEM slot (tcgen05.cp, both
-    // CTAs of the pair) and signals the MMA issuer; issued from its own thread the
-    // copies overlap the issue of the previous stage's MMAs.  The slot is free: the
-    // stage only refills (and its full barrier only completes) after the MMAs that
-    // read the slot have committed.
+    // Move each landed stage's scale atoms into its TMEM slot (tcgen05.cp, both CTAs
+    // of the pair) and signal the MMA issuer.  Issued from their own threads, the
+    // copies overlap the previous stage's MMAs; spread over three warps (SFA, SFB band
+    // 0, SFB band 1), each on its own sub-partition, they overlap best: one warp was
+    // 5 % slower at 8192^3 and 16384^3, four or more (one sharing the MMA warp's
+    // sub-partition) far slower.  The slot is free: the stage only refills (and its
+    // full barrier only completes) after the MMAs that read the slot have committed.
+    const int stream = warp - kSFWarp;  // 0: SFA, 1: SFB band 0, 2: SFB band 1
     if (leader && lane == 0) {
       griddep_wait();
       int stage = 0;
@@ -774,9 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sSFA = sbase + kOffSFA + stage * kSFABytes;
           const uint32_t sSFB = sbase + kOffSFB + stage * kSFBBytes;
           for (int j = 0; j < nk; ++j) {
-            tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
-            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j, make_sdesc(sSFB + j * kAtom, 0, 128, 0));
-            tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4, make_sdesc(sSFB + (kStepsP + j) * kAtom, 0, 128, 0));
+            if (stream == 0)
+              tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+            else
+              tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4 * (stream - 1),
+                                        make_sdesc(sSFB + ((stream - 1) * kStepsP + j) * kAtom, 0, 128, 0));
           }
           tc_commit_pair_mc(bar_sf + 8 * stage, 0x1);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
