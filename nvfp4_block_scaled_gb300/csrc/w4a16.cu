@@ -452,8 +452,10 @@ constexpr int kNumBars = 2 * kMaxRawStages + 2 * kMaxAStages + 2 * kMaxXStages +
 // Shared memory: a ring of 36 KB weight chunks, dequantised A tiles and x tiles.
 // The weight ring is what keeps HBM busy (a chunk takes several microseconds to
 // arrive under load), the A ring decouples dequantisation from the MMAs, and an x
-// slot refills only after the MMA that read it has completed.  Minimums first
-// (2 chunks, 3 A tiles, 3 x tiles), then chunks up to 4, then x tiles up to 16.
+// slot refills only after the MMA that read it has completed.  Two chunks (16 steps
+// of weights) are ahead enough; an x slot is refilled only after the MMA that read
+// it has completed and a copy takes about 1.4 us to land, so x slots get what is
+// left (up to 16), and a fourth A tile when x has 8 slots or more.
 struct Layout {
   int rs, as, xs;
   int off_a, off_x, off_bar, total;
@@ -463,12 +465,11 @@ __host__ __device__ inline Layout layout(int nt) {
   Layout L;
   const int xbytes = nt * 128;
   const int budget = 232448 - 1024 - 8 * kNumBars - 16;
+  L.rs = 2;
   L.as = 3;
-  L.xs = 3;
-  L.rs = (budget - L.as * kABytes - L.xs * xbytes) / kChunkBytes;
-  if (L.rs > kMaxRawStages) L.rs = kMaxRawStages;
   L.xs = (budget - L.as * kABytes - L.rs * kChunkBytes) / xbytes;
   if (L.xs > kMaxXStages) L.xs = kMaxXStages;
+  if (L.xs >= 8 && budget - (L.as + 1) * kABytes - L.rs * kChunkBytes >= L.xs * xbytes) L.as = 4;
   L.off_a = L.rs * kChunkBytes;
   L.off_x = L.off_a + L.as * kABytes;
   L.off_bar = L.off_x + L.xs * xbytes;
@@ -590,19 +591,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();
       const uint32_t idesc = idesc_bf16(128, nt_tok);
       const int n = ks1 - ks0;
+      // Descriptors of slot 0; a slot's (and a K = 16 step's) descriptor is that plus
+      // its byte offset / 16 in the start-address field (shared-memory addresses stay
+      // below 256 KB, so the 14-bit field does not overflow).  A lone issuing thread
+      // is latency-bound, so the per-MMA work is kept to a few adds.
+      const uint64_t a_desc0 = make_sdesc(sbase + L.off_a, 16, 1024, 2);
+      const uint64_t x_desc0 = make_sdesc(sbase + L.off_x, 16, 1024, 2);
+      int as = 0, xs = 0;
+      uint32_t a_ph = 0, x_ph = 0;
       for (int i = 0; i < n; ++i) {
-        const int as = i % AS, xs = i % L.xs;
-        if (!mbar_wait(a_full + 8 * as, (i / AS) & 1, abort_flag)) break;
-        if (!mbar_wait(x_full + 8 * xs, (i / L.xs) & 1, abort_flag)) break;
+        if (!mbar_wait(a_full + 8 * as, a_ph, abort_flag)) break;
+        if (!mbar_wait(x_full + 8 * xs, x_ph, abort_flag)) break;
         tc_fence_after();
-        const uint32_t sa = sbase + L.off_a + as * kABytes;
-        const uint32_t sx = sbase + L.off_x + xs * xbytes;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc_mma_f16(tmem, make_sdesc(sa + 32 * k, 16, 1024, 2), make_sdesc(sx + 32 * k, 16, 1024, 2), idesc,
-                     (i | k) != 0 ? 1u : 0u);
+        const uint64_t ad = a_desc0 + static_cast<uint64_t>(as * (kABytes >> 4));
+        const uint64_t xd = x_desc0 + static_cast<uint64_t>(xs * (xbytes >> 4));
+        tc_mma_f16(tmem, ad, xd, idesc, i != 0 ? 1u : 0u);
+        tc_mma_f16(tmem, ad + 2, xd + 2, idesc, 1u);
+        tc_mma_f16(tmem, ad + 4, xd + 4, idesc, 1u);
+        tc_mma_f16(tmem, ad + 6, xd + 6, idesc, 1u);
         tc_commit(a_empty + 8 * as);
         tc_commit(x_empty + 8 * xs);
+        if (++as == AS) { as = 0; a_ph ^= 1; }
+        if (++xs == L.xs) { xs = 0; x_ph ^= 1; }
       }
       tc_commit(acc_full);
     }
