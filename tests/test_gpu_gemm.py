@@ -133,7 +133,7 @@ def test_gemm_square_sampled(S):
     check_sampled(A, SFA, B, SFB, alpha, D, S, S, 512, f"{S}^3")
 
 
-@pytest.mark.parametrize("S", [16384])
+@pytest.mark.parametrize("S", [16384, 32768])
 def test_gemm_large_square_zero_and_subnormal_scales(S):
     A, SFA, B, SFB = G.gemm_square_inputs(S, S, S, seed=0, scales="zero_sub")
     alpha = G.alpha_uniform(0)
