@@ -744,22 +744,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace tcw
 
-// Split count S (cluster size) and token-tile width for the tensor-core path: tiles
-// = groups x token tiles; S <= 8 splits K when the tiles alone leave SMs idle.
-void choose_tc(int groups, int KC, int M, const DeviceInfo& dev, int* S_out, int* nt_out, int* ttiles_out) {
+// Split count S (cluster size) and token-tile width for the tensor-core path.  A
+// unit (128 weight rows x one token tile) runs as a cluster of S CTAs that split K;
+// active[S] clusters of that size fit on the GPU at once (queried: clusters live
+// inside a GPC, so this is not the SM count / S).  Cost model: waves x (64-K steps
+// per CTA + 8), the 8 standing for a CTA's fixed cost (pipeline fill, drain and
+// the cluster reduction; a globaltimer trace put it near 8 steps).  An earlier
+// wave-fill score that ignored both chose S = 5 for M = 1024 x N = 17408: 2720
+// CTAs of 16 steps each, 2.5x slower than S = 1.
+void choose_tc(int groups, int KC, int M, const int (&active)[9], int* S_out, int* nt_out, int* ttiles_out) {
   const int mt = (M + tcw::kMaxTokens - 1) / tcw::kMaxTokens;     // token tiles
   const int per = (M + mt - 1) / mt;
   const int nt = ((per + 15) / 16) * 16;                          // tokens per tile (multiple of 16)
   const int C = (KC + kChunkKC - 1) / kChunkKC;
-  const double slots = dev.num_sms;
+  const int64_t units = static_cast<int64_t>(groups) * mt;
   int best = 1;
-  double best_score = -1.0;
+  int64_t best_cost = -1;
   for (int S = 1; S <= 8 && S <= C; ++S) {
-    const int maxc = (C + S - 1) / S;
-    const double blocks = static_cast<double>(groups) * mt * S;
-    const double waves = std::ceil(blocks / slots);
-    const double score = ((static_cast<double>(C) / S) / maxc) * (blocks / (waves * slots)) / (1.0 + 0.02 * (S - 1));
-    if (score > best_score + 1e-9) { best_score = score; best = S; }
+    const int64_t act = active[S] > 0 ? active[S] : 1;
+    const int64_t waves = (units + act - 1) / act;
+    const int64_t steps = (static_cast<int64_t>((C + S - 1) / S)) * kChunkKC;
+    const int64_t cost = waves * (steps + 8);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = S; }
   }
   *S_out = best;
   *nt_out = nt;
@@ -768,23 +774,40 @@ void choose_tc(int groups, int KC, int M, const DeviceInfo& dev, int* S_out, int
 
 nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, __nv_bfloat16* y, int M, int N, int K,
                        cudaStream_t stream, const DeviceInfo& dev) {
+  auto kern = tcw::w4a16_tc_kernel;
+  static bool attr_set[64] = {};
+  static int active[64][9] = {};  // co-resident clusters of S CTAs (one CTA per SM), per device
+  const int d = dev.device < 64 ? dev.device : 63;
+  if (!attr_set[d]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dev.max_smem_optin)) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    for (int s = 1; s <= 8; ++s) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(s, 1, 1);
+      qc.blockDim = dim3(tcw::kThreads, 1, 1);
+      qc.dynamicSmemBytes = static_cast<size_t>(tcw::layout(tcw::kMaxTokens).total);
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = s;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess) n = 0;
+      active[d][s] = n > 0 ? n : dev.num_sms / s;
+    }
+    attr_set[d] = true;
+  }
   int S, nt, mt;
-  choose_tc(N / 128, K / 64, M, dev, &S, &nt, &mt);
+  choose_tc(N / 128, K / 64, M, active[d], &S, &nt, &mt);
   const tcw::Layout L = tcw::layout(nt);
   if (L.rs < 2 || L.xs < 3 || static_cast<size_t>(L.total) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (S > 1 && nt * 128 * 4 > L.off_bar) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap tmX;
   nvfp4_status st = encode_tmap_x_blocks(&tmX, x, M, K, static_cast<uint32_t>(nt), 1);
   if (st != NVFP4_OK) return st;
-  auto kern = tcw::w4a16_tc_kernel;
-  static bool attr_set[64] = {};
-  const int d = dev.device < 64 ? dev.device : 63;
-  if (!attr_set[d]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(dev.max_smem_optin)) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    attr_set[d] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, N / 128, mt);
   cfg.blockDim = dim3(tcw::kThreads, 1, 1);
