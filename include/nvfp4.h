@@ -22,6 +22,12 @@
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronises the host.  Calls on different streams may run
  *     concurrently.
+ *   - Every kernel is launched with programmatic dependent launch allowed: a call
+ *     may start (and stream its weight operand) while the previous kernel in the
+ *     stream is still running, and waits for that kernel to complete before it
+ *     reads activations or writes its output.  A caller's own kernel launched after
+ *     one of these with programmatic stream serialization must likewise wait
+ *     (griddepcontrol.wait / cudaGridDependencySynchronize) before reading the output.
  *   - Errors are returned as nvfp4_status; nothing aborts or throws.  Arguments are
  *     checked on the host; device data (codes, scales) is NOT validated: a NaN
  *     (0x7F/0xFF) or negative scale byte given to nvfp4_gemm gives undefined
@@ -185,6 +191,23 @@ nvfp4_status nvfp4_w4a16_prepare(const uint8_t* W_codes, const uint8_t* W_sf_row
  */
 nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alpha, void* y_bf16,
                                 int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_w4a16_linear_colscale -- nvfp4_w4a16_linear with one FP32 weight scale per
+ * output column instead of the global alpha:
+ *
+ *     y[m, n] = bf16(alpha_col[n] * sum_k x[m, k] * dequant(W)[n, k]),  FP32 accumulation.
+ *
+ * [P2] Design: the weight carries "global or per-column scale".  Same kernels,
+ * arguments and rules as nvfp4_w4a16_linear, except:
+ *   alpha_col  [N] FP32, DEVICE pointer owned by the caller, 16-byte aligned; read
+ *              once per output element (finite values assumed, not checked).
+ * Accuracy: |y - exact| <= 2^-8 |exact| + 1e-6 |alpha_col[n]| sum_k |x_k w_k|.
+ * Errors: NVFP4_ERR_INVALID_ARG for a NULL alpha_col, NVFP4_ERR_MISALIGNED if it is
+ * not 16-byte aligned, otherwise as nvfp4_w4a16_linear.
+ */
+nvfp4_status nvfp4_w4a16_linear_colscale(const void* x_bf16, const void* Wprep, const float* alpha_col,
+                                         void* y_bf16, int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream);
 
 /*
  * nvfp4_device_error -- synchronise `stream`, then read the device-side error word

@@ -9,7 +9,7 @@ no CPU fallback: if the shared library has not been built, the first call raises
 Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
   quantize, packed_scales_bytes, pack_scales, gemm, gemm_config_name,
   gemm_choose_config, w4a16_prepared_bytes, w4a16_prepare, w4a16_linear,
-  device_error.
+  w4a16_linear_colscale, device_error.
 """
 
 from __future__ import annotations
@@ -24,7 +24,7 @@ ABI_SYMBOLS = (
     "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_packed_scales_bytes",
     "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
-    "nvfp4_w4a16_linear", "nvfp4_device_error",
+    "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_device_error",
 )
 
 NVFP4_OK = 0
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_w4a16_prepared_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
         "nvfp4_w4a16_prepare": (c_i, [c_p, c_p, c_i64, c_i64, c_p, c_p]),
         "nvfp4_w4a16_linear": (c_i, [c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
+        "nvfp4_w4a16_linear_colscale": (c_i, [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_device_error": (c_i, [c_p, c_i]),
     }
     for name, (res, args) in sig.items():
@@ -219,6 +220,24 @@ def w4a16_linear(x, Wprep, alpha: float, N: int, out=None, stream=None):
     _cuda(out, "out", torch.bfloat16)
     _check("nvfp4_w4a16_linear", load_library().nvfp4_w4a16_linear(
         _ptr(x), _ptr(Wprep), float(alpha), _ptr(out), M, int(N), K, _stream(stream)))
+    return out
+
+
+def w4a16_linear_colscale(x, Wprep, alpha_col, N: int, out=None, stream=None):
+    """y = bf16(alpha_col[n] * x * dequant(W)^T); alpha_col float32 [N] on the device."""
+    import torch
+
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(Wprep, "Wprep", torch.uint8)
+    _cuda(alpha_col, "alpha_col", torch.float32)
+    if alpha_col.numel() != N:
+        raise ValueError(f"alpha_col holds {alpha_col.numel()} scales, needs {N}")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("nvfp4_w4a16_linear_colscale", load_library().nvfp4_w4a16_linear_colscale(
+        _ptr(x), _ptr(Wprep), _ptr(alpha_col), _ptr(out), M, int(N), K, _stream(stream)))
     return out
 
 

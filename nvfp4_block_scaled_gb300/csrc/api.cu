@@ -251,18 +251,37 @@ nvfp4_status nvfp4_w4a16_prepare(const uint8_t* W_codes, const uint8_t* W_sf_row
   return launch_w4a16_prepare(W_codes, W_sf_rowmajor, N, K, Wprep, as_stream(stream), dev);
 }
 
-nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alpha, void* y_bf16, int64_t M,
-                                int64_t N, int64_t K, nvfp4_stream_t stream) {
+static nvfp4_status w4a16_checks(const void* x_bf16, const void* Wprep, void* y_bf16, int64_t M, int64_t N,
+                                 int64_t K) {
   if (x_bf16 == nullptr || Wprep == nullptr || y_bf16 == nullptr) return NVFP4_ERR_INVALID_ARG;
   if (M < 1 || N < 128 || K < 256 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
-  if (!(alpha == alpha) || alpha > 3.4028234663852886e38f || alpha < -3.4028234663852886e38f)
-    return NVFP4_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(x_bf16, 16) || !aligned(Wprep, 16) || !aligned(y_bf16, 16)) return NVFP4_ERR_MISALIGNED;
-  DeviceInfo dev;
-  nvfp4_status st = current_device(&dev);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alpha, void* y_bf16, int64_t M,
+                                int64_t N, int64_t K, nvfp4_stream_t stream) {
+  nvfp4_status st = w4a16_checks(x_bf16, Wprep, y_bf16, M, N, K);
   if (st != NVFP4_OK) return st;
-  return launch_w4a16_linear(x_bf16, Wprep, alpha, y_bf16, M, N, K, as_stream(stream), dev);
+  if (!(alpha == alpha) || alpha > 3.4028234663852886e38f || alpha < -3.4028234663852886e38f)
+    return NVFP4_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_w4a16_linear(x_bf16, Wprep, alpha, nullptr, y_bf16, M, N, K, as_stream(stream), dev);
+}
+
+nvfp4_status nvfp4_w4a16_linear_colscale(const void* x_bf16, const void* Wprep, const float* alpha_col,
+                                         void* y_bf16, int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream) {
+  nvfp4_status st = w4a16_checks(x_bf16, Wprep, y_bf16, M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (alpha_col == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(alpha_col, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_w4a16_linear(x_bf16, Wprep, 1.0f, alpha_col, y_bf16, M, N, K, as_stream(stream), dev);
 }
 
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear) {

@@ -76,7 +76,8 @@ nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const
 
 nvfp4_status launch_w4a16_prepare(const uint8_t* W, const uint8_t* SW, int64_t N, int64_t K, void* Wprep,
                                   cudaStream_t stream, const DeviceInfo& dev);
-nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, void* y, int64_t M,
-                                 int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+// alpha_col: NULL for the global scale alpha, else N per-output-column FP32 scales.
+nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, const float* alpha_col, void* y,
+                                 int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);
 
 }  // namespace nvfp4

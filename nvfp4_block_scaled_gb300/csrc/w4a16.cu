@@ -183,7 +183,8 @@ constexpr int decode_min_blocks() { return MT <= 2 ? 2 : 1; }
 template <int MT>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
     w4a16_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                        float alpha128, __nv_bfloat16* __restrict__ y, int M, int N, int K, int S) {
+                        float alpha128, const float* __restrict__ alpha_col, __nv_bfloat16* __restrict__ y, int M,
+                        int N, int K, int S) {
   constexpr int Mpad = 8 * MT;
   constexpr int kStage = decode_stage_bytes(Mpad);
   constexpr int kStageTx = kStage;
@@ -358,7 +359,9 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
         sum += v[2 * src + 1];
       }
     }
-    y[static_cast<size_t>(tok) * N + static_cast<size_t>(grp) * 128 + row] = __float2bfloat16_rn(sum * alpha128);
+    // alpha * 2^7 (the weights carry 2^-7); a per-column alpha times 128 is exact too
+    const float sc = alpha_col != nullptr ? alpha_col[grp * 128 + row] * 128.0f : alpha128;
+    y[static_cast<size_t>(tok) * N + static_cast<size_t>(grp) * 128 + row] = __float2bfloat16_rn(sum * sc);
   }
   cluster_sync_all();
 }
@@ -387,8 +390,8 @@ int choose_split(int groups, int KC, int MT, const DeviceInfo& dev) {
 }
 
 template <int MT>
-nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float alpha128, __nv_bfloat16* y, int M,
-                           int N, int K, int S, cudaStream_t stream, const DeviceInfo& dev) {
+nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float alpha128, const float* alpha_col,
+                           __nv_bfloat16* y, int M, int N, int K, int S, cudaStream_t stream, const DeviceInfo& dev) {
   auto kern = w4a16_decode_kernel<MT>;
   const int smem = decode_smem_bytes(8 * MT);
   if (static_cast<size_t>(smem) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_DEVICE;
@@ -418,7 +421,7 @@ nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S));
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, alpha_col, y, M, N, K, S));
 }
 
 // ------------------------------------------------------------------ linear (tensor cores)
@@ -490,7 +493,8 @@ __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    float alpha128, __nv_bfloat16* __restrict__ y, int M, int N, int K, int S, int nt_tok) {
+                    float alpha128, const float* __restrict__ alpha_col, __nv_bfloat16* __restrict__ y, int M,
+                    int N, int K, int S, int nt_tok) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
@@ -673,6 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q = warp & 3;  // TMEM lane quarter this warp may access
       const int row = 32 * q + lane;
       const int mv = min(nt_tok, M - m0);
+      const float sc = alpha_col != nullptr ? alpha_col[grp * 128 + row] * 128.0f : alpha128;
       if (warp_wait(acc_full, 0, abort_flag)) {
         tc_fence_after();
         float* part = reinterpret_cast<float*>(smem);  // [tokens][128 rows], after the loop
@@ -687,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tok < mv) {
               if (S == 1)
                 y[static_cast<size_t>(m0 + tok) * N + static_cast<size_t>(grp) * 128 + row] =
-                    __float2bfloat16_rn(__uint_as_float(v[jj]) * alpha128);
+                    __float2bfloat16_rn(__uint_as_float(v[jj]) * sc);
               else
                 part[tok * 128 + row] = __uint_as_float(v[jj]);
             }
@@ -726,8 +731,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           sum.w += v[src].w;
         }
       }
-      __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x * alpha128, sum.y * alpha128);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z * alpha128, sum.w * alpha128);
+      float4 sc = make_float4(alpha128, alpha128, alpha128, alpha128);
+      if (alpha_col != nullptr) {
+        const float4 a = *reinterpret_cast<const float4*>(alpha_col + grp * 128 + row);
+        sc = make_float4(a.x * 128.0f, a.y * 128.0f, a.z * 128.0f, a.w * 128.0f);
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x * sc.x, sum.y * sc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z * sc.z, sum.w * sc.w);
       uint2 packed;
       packed.x = *reinterpret_cast<uint32_t*>(&lo);
       packed.y = *reinterpret_cast<uint32_t*>(&hi);
@@ -772,8 +782,8 @@ void choose_tc(int groups, int KC, int M, const int (&active)[9], int* S_out, in
   *ttiles_out = mt;
 }
 
-nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, __nv_bfloat16* y, int M, int N, int K,
-                       cudaStream_t stream, const DeviceInfo& dev) {
+nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, const float* alpha_col, __nv_bfloat16* y,
+                       int M, int N, int K, cudaStream_t stream, const DeviceInfo& dev) {
   auto kern = tcw::w4a16_tc_kernel;
   static bool attr_set[64] = {};
   static int active[64][9] = {};  // co-resident clusters of S CTAs (one CTA per SM), per device
@@ -822,7 +832,7 @@ nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, __
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, y, M, N, K, S, nt));
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, alpha_col, y, M, N, K, S, nt));
 }
 
 }  // namespace
@@ -847,8 +857,8 @@ nvfp4_status launch_w4a16_prepare(const uint8_t* W, const uint8_t* SW, int64_t N
   return from_cuda(cudaGetLastError());
 }
 
-nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, void* y, int64_t M, int64_t N,
-                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, const float* alpha_col, void* y,
+                                 int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
   const float alpha128 = alpha * 128.0f;
   const int KC = static_cast<int>(K / 64);
   const int groups = static_cast<int>(N / 128);
@@ -865,8 +875,8 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
   // which streams at a higher rate there -- the tensor-core path recycles each A
   // tile through an MMA commit (about a microsecond), and shared memory holds too
   // few tiles to hide that at decode-sized MMAs.
-  if (M > 32) return launch_tc(tmW, xb, alpha128, yb, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                               stream, dev);
+  if (M > 32) return launch_tc(tmW, xb, alpha128, alpha_col, yb, static_cast<int>(M), static_cast<int>(N),
+                               static_cast<int>(K), stream, dev);
   // Token chunks of up to 32 rows per launch.
   for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxTokens) {
     const int mc = static_cast<int>(M - m0 < kDecodeMaxTokens ? M - m0 : kDecodeMaxTokens);
@@ -877,9 +887,9 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
     if (st != NVFP4_OK) return st;
     __nv_bfloat16* yc = yb + m0 * N;
     switch (MT) {
-      case 1: st = launch_decode<1>(tmW, tmX, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
-      case 2: st = launch_decode<2>(tmW, tmX, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
-      default: st = launch_decode<4>(tmW, tmX, alpha128, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
+      case 1: st = launch_decode<1>(tmW, tmX, alpha128, alpha_col, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
+      case 2: st = launch_decode<2>(tmW, tmX, alpha128, alpha_col, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
+      default: st = launch_decode<4>(tmW, tmX, alpha128, alpha_col, yc, mc, static_cast<int>(N), static_cast<int>(K), S, stream, dev); break;
     }
     if (st != NVFP4_OK) return st;
   }

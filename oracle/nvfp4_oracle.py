@@ -325,6 +325,19 @@ def w4a16_linear(x_bf16_bits, W, SW, alpha: float):
     return ref, abs_sum
 
 
+def w4a16_linear_colscale(x_bf16_bits, W, SW, alpha_col):
+    """Per-column weight scale ([P2] Design: "global or per-column scale"):
+    y[m, n] = alpha_col[n] * sum_k x[m, k] * w[n, k].  Returns (ref, scaled_abs_sum),
+    float64 [M, N], where scaled_abs_sum[m, n] = |alpha_col[n]| * sum_k |x w|, so
+    that ``tolerance(ref, scaled_abs_sum, 1.0)`` is the per-element bound."""
+    x = bf16_bits_to_f64(x_bf16_bits)
+    w = dequantize(W, SW)
+    a = np.asarray(alpha_col, dtype=np.float64).reshape(1, -1)
+    ref = (x @ w.T) * a
+    abs_sum = (np.abs(x) @ np.abs(w).T) * np.abs(a)
+    return ref, abs_sum
+
+
 def w4a16_linear_at(x_bf16_bits, W, SW, alpha: float, rows, cols):
     rows = np.asarray(rows, dtype=np.int64)
     cols = np.asarray(cols, dtype=np.int64)

@@ -173,3 +173,51 @@ def test_linear_graph_replay_matches_eager(M):
     assert nv.device_error() == 0
     assert torch.equal(y1.view(torch.int16), e1.view(torch.int16))
     assert torch.equal(y2.view(torch.int16), e2.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (17, 384, 1024), (32, 256, 4096), (72, 256, 512),
+                                   (40, 384, 768), (300, 256, 1280)])
+def test_linear_colscale(M, N, K):
+    # One FP32 scale per output column (negative, zero and non-power-of-two values),
+    # through the decode kernel (M <= 32, cluster K split) and the tensor-core path
+    # (M > 32, with and without its cluster reduction).
+    x = G.bf16_normal(M, K, M + 3, "x")
+    W = G.packed_codes_uniform(N, K, M + 3, "W")
+    SW = G.scales_with_zero_and_subnormal(N, K, M + 3, "SW", 0.05, 0.05)
+    SW = np.where(np.random.default_rng(M).random(SW.shape) < 0.1, SW | 0x80, SW).astype(np.uint8)
+    alpha = np.random.default_rng(N + M).uniform(-4.0, 4.0, N).astype(np.float32)
+    alpha[::17] = 0.0
+    wp = nv.w4a16_prepare(dev(W), dev(SW))
+    y = nv.w4a16_linear_colscale(dev_bf16(x), wp, dev(alpha), N)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    ref, sabs = O.w4a16_linear_colscale(x, W, SW, alpha)
+    assert_within(host_f64(y), ref, sabs, 1.0, f"w4a16 colscale {M}x{N}x{K}")
+
+
+def test_linear_colscale_rejects_bad_scale_pointer():
+    x = torch.zeros((1, 256), dtype=torch.bfloat16, device="cuda")
+    wp = torch.zeros(nv.w4a16_prepared_bytes(128, 256), dtype=torch.uint8, device="cuda")
+    y = torch.empty((1, 128), dtype=torch.bfloat16, device="cuda")
+    lib = nv.load_library()
+    st = lib.nvfp4_w4a16_linear_colscale(x.data_ptr(), wp.data_ptr(), None, y.data_ptr(), 1, 128, 256,
+                                         torch.cuda.current_stream().cuda_stream)
+    assert st == -1
+    a = torch.ones(129, dtype=torch.float32, device="cuda")
+    st = lib.nvfp4_w4a16_linear_colscale(x.data_ptr(), wp.data_ptr(), a.data_ptr() + 4, y.data_ptr(), 1, 128, 256,
+                                         torch.cuda.current_stream().cuda_stream)
+    assert st == -3
+
+
+def test_linear_more_than_1024_tokens():
+    # [P2] runs M > 1024 as 1024-row chunks; here token tiles of at most 256 cover
+    # any M in one launch.
+    M, N, K = 1300, 256, 512
+    x = G.bf16_normal(M, K, 8, "x")
+    W = G.packed_codes_uniform(N, K, 8, "W")
+    SW = G.scales_uniform_normal(N, K, 8, "SW")
+    wp = nv.w4a16_prepare(dev(W), dev(SW))
+    y = nv.w4a16_linear(dev_bf16(x), wp, 0.75, N)
+    torch.cuda.synchronize()
+    ref, abs_sum = O.w4a16_linear(x, W, SW, 0.75)
+    assert_within(host_f64(y), ref, abs_sum, 0.75, "w4a16 M=1300")

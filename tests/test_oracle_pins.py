@@ -371,3 +371,28 @@ def test_w4a16_sampled_agrees_with_full():
     ref, abs_sum = O.w4a16_linear(x, W, SW, 2.0)
     r, a = O.w4a16_linear_at(x, W, SW, 2.0, [0, 4, 2], [31, 0, 7])
     assert np.allclose(r, ref[[0, 4, 2], [31, 0, 7]], rtol=1e-15, atol=0)
+
+
+def test_w4a16_colscale_equals_exact_rational_brute_force():
+    # Per-column weight scale: y[m, n] = alpha_n * sum_k x w, checked against exact
+    # rationals with distinct alphas per column (negative, zero, non-power-of-two).
+    M, N, K = 3, 16, 64
+    x = G.bf16_normal(M, K, 7, "x")
+    W = G.packed_codes_uniform(N, K, 7, "W")
+    SW = G.scales_with_zero_and_subnormal(N, K, 7, "SW", 0.1, 0.2)
+    alpha = np.array([0.375 * (n - 5) + (0.1 if n % 3 == 0 else 0.0) for n in range(N)], np.float32)
+    alpha[4] = 0.0
+    ref, sabs = O.w4a16_linear_colscale(x, W, SW, alpha)
+    xf = [[Fraction(float(v)) for v in row] for row in O.bf16_bits_to_f64(x)]
+    w = _frac_dequant(W, SW)
+    for m in range(M):
+        for n in range(N):
+            a = Fraction(float(alpha[n]))
+            s = sum(xf[m][k] * w[n][k] for k in range(K))
+            sa = sum(abs(xf[m][k] * w[n][k]) for k in range(K))
+            assert abs(Fraction(ref[m, n]) - a * s) <= Fraction(1, 2 ** 40) * (1 + abs(a * s))
+            assert abs(Fraction(sabs[m, n]) - abs(a) * sa) <= Fraction(1, 2 ** 40) * (1 + abs(a) * sa)
+    # A constant column scale is the global-scale case, whose own pin is above.
+    r1, a1 = O.w4a16_linear_colscale(x, W, SW, np.full(N, 0.5, np.float32))
+    r2, a2 = O.w4a16_linear(x, W, SW, 0.5)
+    assert np.array_equal(r1, r2) and np.array_equal(a1 * 1.0, a2 * 0.5)
