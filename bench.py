@@ -487,7 +487,11 @@ def bench_producers(peaks):
     sfs = [torch.empty((R, K // 16), dtype=torch.uint8, device="cuda") for _ in range(n)]
     calls = [lambda st, i=i: nv.quantize(xs[i], g, codes[i], sfs[i], stream=st) for i in range(n)]
     res["quantize"] = graph_time(calls, qbytes)
-    del xs, codes
+    # fused quantize + pack: same reads, scales written in the packed layout
+    sfps = [torch.empty(nv.packed_scales_bytes(R, K), dtype=torch.uint8, device="cuda") for _ in range(n)]
+    calls = [lambda st, i=i: nv.quantize_packed(xs[i], g, codes[i], sfps[i], stream=st) for i in range(n)]
+    res["quantize_packed"] = graph_time(calls, qbytes)
+    del xs, codes, sfps
     # pack_scales: 1 B in, 1 B out per scale
     pbytes = 2 * R * K // 16
     n = max(2, int(np.ceil(4 * l2 / pbytes)))

@@ -93,6 +93,20 @@ nvfp4_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t K, float g
                             uint8_t* codes, uint8_t* sf_rowmajor, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_packed -- nvfp4_quantize with the scales written straight into the
+ * packed 128x4-atom layout the GEMM reads (the result of nvfp4_pack_scales on
+ * nvfp4_quantize's row-major scales, byte for byte, padding included), so that an
+ * activation goes quantize -> GEMM with no separate packing pass.
+ *
+ *   x_bf16, rows, K, global_scale, codes   as nvfp4_quantize.
+ *   sf_packed   nvfp4_packed_scales_bytes(rows, K) bytes out, 16-byte aligned;
+ *               padding rows and padding micro-blocks are written as zero.
+ * Errors as nvfp4_quantize, plus NVFP4_ERR_MISALIGNED for a misaligned sf_packed.
+ */
+nvfp4_status nvfp4_quantize_packed(const void* x_bf16, int64_t rows, int64_t K, float global_scale,
+                                   uint8_t* codes, uint8_t* sf_packed, nvfp4_stream_t stream);
+
+/*
  * Size in bytes of the packed scale-factor buffer of a [rows x K] operand:
  * ceil(rows/128)*128 * ceil(K/64)*4.  Returns 0 for rows < 1 or K < 16 or K % 16 != 0.
  */

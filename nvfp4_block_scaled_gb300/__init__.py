@@ -7,7 +7,7 @@ CUDA stream to the C ABI, and raise ``NVFP4Error`` on a non-OK status.  There is
 no CPU fallback: if the shared library has not been built, the first call raises.
 
 Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
-  quantize, packed_scales_bytes, pack_scales, gemm, gemm_config_name,
+  quantize, quantize_packed, packed_scales_bytes, pack_scales, gemm, gemm_config_name,
   gemm_choose_config, w4a16_prepared_bytes, w4a16_prepare, w4a16_linear,
   w4a16_linear_colscale, device_error.
 """
@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 
 #: Every symbol include/nvfp4.h declares.
 ABI_SYMBOLS = (
-    "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_packed_scales_bytes",
+    "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_quantize_packed", "nvfp4_packed_scales_bytes",
     "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
     "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_device_error",
@@ -55,6 +55,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_status_string": (ctypes.c_char_p, [c_i]),
         "nvfp4_version": (c_i, []),
         "nvfp4_quantize": (c_i, [c_p, c_i64, c_i64, c_f, c_p, c_p, c_p]),
+        "nvfp4_quantize_packed": (c_i, [c_p, c_i64, c_i64, c_f, c_p, c_p, c_p]),
         "nvfp4_packed_scales_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
         "nvfp4_pack_scales": (c_i, [c_p, c_i64, c_i64, c_p, c_p]),
         "nvfp4_gemm": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
@@ -136,6 +137,26 @@ def quantize(x, global_scale: float, codes=None, sf=None, stream=None):
     _check("nvfp4_quantize", load_library().nvfp4_quantize(
         _ptr(x), rows, K, float(global_scale), _ptr(codes), _ptr(sf), _stream(stream)))
     return codes, sf
+
+
+def quantize_packed(x, global_scale: float, codes=None, sf_packed=None, stream=None):
+    """bf16 [rows, K] -> (codes uint8 [rows, K/2], packed scales uint8 [packed_scales_bytes])."""
+    import torch
+
+    _cuda(x, "x", torch.bfloat16)
+    rows, K = x.shape
+    n = packed_scales_bytes(rows, K)
+    if codes is None:
+        codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+    if sf_packed is None:
+        sf_packed = torch.empty((n,), dtype=torch.uint8, device=x.device)
+    _cuda(codes, "codes", torch.uint8)
+    _cuda(sf_packed, "sf_packed", torch.uint8)
+    if sf_packed.numel() < n:
+        raise ValueError(f"sf_packed holds {sf_packed.numel()} bytes, needs {n}")
+    _check("nvfp4_quantize_packed", load_library().nvfp4_quantize_packed(
+        _ptr(x), rows, K, float(global_scale), _ptr(codes), _ptr(sf_packed), _stream(stream)))
+    return codes, sf_packed
 
 
 def pack_scales(sf, K: int | None = None, out=None, stream=None):

@@ -163,17 +163,35 @@ const char* nvfp4_status_string(int status) {
 
 int nvfp4_version(void) { return 10000; }
 
-nvfp4_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t K, float global_scale, uint8_t* codes,
-                            uint8_t* sf_rowmajor, nvfp4_stream_t stream) {
-  if (x_bf16 == nullptr || codes == nullptr || sf_rowmajor == nullptr) return NVFP4_ERR_INVALID_ARG;
+static nvfp4_status quantize_checks(const void* x_bf16, int64_t rows, int64_t K, float global_scale,
+                                    const uint8_t* codes, const uint8_t* sf) {
+  if (x_bf16 == nullptr || codes == nullptr || sf == nullptr) return NVFP4_ERR_INVALID_ARG;
   if (rows < 1 || K < 16 || rows > kMaxDim || K > kMaxDim) return NVFP4_ERR_INVALID_ARG;
   if (!(global_scale > 0.0f) || !(global_scale <= 3.4028234663852886e38f)) return NVFP4_ERR_INVALID_ARG;
   if (K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(x_bf16, 16) || !aligned(codes, 8)) return NVFP4_ERR_MISALIGNED;
-  DeviceInfo dev;
-  nvfp4_status st = current_device(&dev);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t K, float global_scale, uint8_t* codes,
+                            uint8_t* sf_rowmajor, nvfp4_stream_t stream) {
+  nvfp4_status st = quantize_checks(x_bf16, rows, K, global_scale, codes, sf_rowmajor);
   if (st != NVFP4_OK) return st;
-  return launch_quantize(x_bf16, rows, K, global_scale, codes, sf_rowmajor, as_stream(stream), dev);
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_quantize(x_bf16, rows, K, global_scale, codes, sf_rowmajor, false, as_stream(stream), dev);
+}
+
+nvfp4_status nvfp4_quantize_packed(const void* x_bf16, int64_t rows, int64_t K, float global_scale,
+                                   uint8_t* codes, uint8_t* sf_packed, nvfp4_stream_t stream) {
+  nvfp4_status st = quantize_checks(x_bf16, rows, K, global_scale, codes, sf_packed);
+  if (st != NVFP4_OK) return st;
+  if (!aligned(sf_packed, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_quantize(x_bf16, rows, K, global_scale, codes, sf_packed, true, as_stream(stream), dev);
 }
 
 size_t nvfp4_packed_scales_bytes(int64_t rows, int64_t K) {

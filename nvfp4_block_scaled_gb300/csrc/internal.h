@@ -62,8 +62,10 @@ int read_device_error_gemm(bool clear);
 int read_device_error_w4a16(bool clear);
 
 // Kernel launchers (defined next to their kernels).
+// packed = false: sf is [rows x K/16] row-major; true: sf is the packed 128x4-atom
+// buffer of nvfp4_packed_scales_bytes(rows, K) bytes, padding written as zero.
 nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, uint8_t* codes,
-                             uint8_t* sf, cudaStream_t stream, const DeviceInfo& dev);
+                             uint8_t* sf, bool packed, cudaStream_t stream, const DeviceInfo& dev);
 nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
 

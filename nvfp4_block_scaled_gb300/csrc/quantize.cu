@@ -3,7 +3,8 @@
 //
 // Both kernels are HBM-bound: quantize takes one 16-element block per thread
 // (coalesced 32-byte loads, 8-byte code stores) over a grid sized to a multiple of
-// the SM count; pack_scales transposes 128-row bands through shared memory.
+// the SM count, and can write its scales straight into the packed layout (fused
+// quantize + pack); pack_scales transposes 128-row bands through shared memory.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -39,6 +40,41 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
   return r;
 }
 
+// Quantise one 16-element block: v0, v1 = its 32 bytes of bf16.  Returns the E4M3
+// scale byte and writes the 16 codes (little-endian nibbles) to *c0, *c1.
+__device__ __forceinline__ uint32_t quantize_block(uint4 v0, uint4 v1, float g, uint32_t* c0_out,
+                                                   uint32_t* c1_out) {
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const float s = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+  const uint32_t sbyte = __nv_cvt_float_to_fp8(s, __NV_SATFINITE, __NV_E4M3);
+  uint32_t c0 = 0, c1 = 0;
+  if (sbyte != 0) {
+    const float denom = __fmul_rn(e4m3_to_float(sbyte), g);
+    float q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(f[i], denom);
+    c0 = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+    c1 = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+    // A code whose magnitude rounded to zero is written as +0 (clear its sign bit).
+    const uint32_t nz0 = ((c0 & 0x77777777u) + 0x77777777u) & 0x88888888u;
+    const uint32_t nz1 = ((c1 & 0x77777777u) + 0x77777777u) & 0x88888888u;
+    c0 &= 0x77777777u | nz0;
+    c1 &= 0x77777777u | nz1;
+  }
+  *c0_out = c0;
+  *c1_out = c1;
+  return sbyte;
+}
+
 __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t nblocks,
                                                        float g, uint2* __restrict__ codes,
                                                        uint8_t* __restrict__ sf) {
@@ -46,36 +82,64 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
   griddep_launch_dependents();   // a following GEMM may start streaming its weights
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
-    const uint4 v0 = __ldcs(x + 2 * b);
-    const uint4 v1 = __ldcs(x + 2 * b + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float f[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    const float s = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
-    const uint32_t sbyte = __nv_cvt_float_to_fp8(s, __NV_SATFINITE, __NV_E4M3);
-    uint32_t c0 = 0, c1 = 0;
-    if (sbyte != 0) {
-      const float denom = __fmul_rn(e4m3_to_float(sbyte), g);
-      float q[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(f[i], denom);
-      c0 = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-      c1 = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
-      // A code whose magnitude rounded to zero is written as +0 (clear its sign bit).
-      const uint32_t nz0 = ((c0 & 0x77777777u) + 0x77777777u) & 0x88888888u;
-      const uint32_t nz1 = ((c1 & 0x77777777u) + 0x77777777u) & 0x88888888u;
-      c0 &= 0x77777777u | nz0;
-      c1 &= 0x77777777u | nz1;
-    }
+    uint32_t c0, c1;
+    const uint32_t sbyte = quantize_block(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), g, &c0, &c1);
     __stcs(codes + b, make_uint2(c0, c1));
     sf[b] = static_cast<uint8_t>(sbyte);
+  }
+}
+
+// Fused quantize + pack.  One thread block of 16 warps per (128-row band, 8 atoms
+// = 32 scale columns): warp w quantises rows w, w+16, ..., w+112 of the band, lane
+// l the block in scale column 32*tile + l of each (a warp reads 1 KB and writes 256
+// bytes of codes contiguously).  Two shuffles assemble each 4-scale word of an
+// atom into a shared-memory tile, which is then written atom by atom, 512
+// contiguous bytes each (word w of an atom holds row 32*(w%4) + w/4): scattered
+// single-byte scale stores in the layout cost more than the separate packing pass.
+// Rows past `rows` and scale columns past C give zero scale bytes and no codes.
+// (16 warps per block: the quantiser is bound by chains of IEEE divisions, so it
+// wants the SM's full 64 warps.)
+constexpr int kQPAtoms = 8;
+constexpr int kQPPitch = kQPAtoms + 1;  // words per tile row (odd: spreads the banks)
+constexpr int kQPThreads = 512;
+
+__global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                     int64_t C, int64_t groups, int64_t tiles_per_band,
+                                                                     int64_t num_tiles, float g,
+                                                                     uint2* __restrict__ codes,
+                                                                     uint32_t* __restrict__ sf_packed) {
+  __shared__ uint32_t tile[128 * kQPPitch];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const int64_t band = t / tiles_per_band;
+    const int64_t a0 = (t - band * tiles_per_band) * kQPAtoms;
+    const int na = static_cast<int>(groups - a0 < kQPAtoms ? groups - a0 : kQPAtoms);
+    const int64_t c = 4 * a0 + lane;
+    const bool col_ok = c < C;
+#pragma unroll
+    for (int rr = 0; rr < 128 / (kQPThreads / 32); ++rr) {
+      const int row = warp + (kQPThreads / 32) * rr;
+      const int64_t r = band * 128 + row;
+      uint32_t sbyte = 0;
+      if (col_ok && r < rows) {
+        const int64_t b = r * C + c;
+        uint32_t c0, c1;
+        sbyte = quantize_block(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), g, &c0, &c1);
+        __stcs(codes + b, make_uint2(c0, c1));
+      }
+      const uint32_t w1 = sbyte | (__shfl_down_sync(0xffffffffu, sbyte, 1) << 8);
+      const uint32_t w2 = w1 | (__shfl_down_sync(0xffffffffu, w1, 2) << 16);
+      if ((lane & 3) == 0) tile[row * kQPPitch + (lane >> 2)] = w2;
+    }
+    __syncthreads();
+    uint32_t* dst = sf_packed + (band * groups + a0) * 128;
+    for (int i = threadIdx.x; i < na * 128; i += blockDim.x) {
+      const int a = i >> 7, wd = i & 127;
+      dst[i] = tile[(32 * (wd & 3) + (wd >> 2)) * kQPPitch + a];
+    }
+    __syncthreads();
   }
 }
 
@@ -168,14 +232,24 @@ int grid_for(int64_t work_items, int threads, const DeviceInfo& dev, int per_sm)
 }  // namespace
 
 nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, uint8_t* codes, uint8_t* sf,
-                             cudaStream_t stream, const DeviceInfo& dev) {
-  const int64_t nblocks = rows * (K / 16);
-  const int grid = grid_for(nblocks, 256, dev, 8);
-  cudaLaunchConfig_t cfg = programmatic_config(grid, 256, stream);
+                             bool packed, cudaStream_t stream, const DeviceInfo& dev) {
+  const int64_t C = K / 16;
   cudaLaunchAttribute attr[1];
+  if (!packed) {
+    const int64_t nblocks = rows * C;
+    cudaLaunchConfig_t cfg = programmatic_config(grid_for(nblocks, 256, dev, 8), 256, stream);
+    set_programmatic(cfg, attr);
+    return from_cuda(cudaLaunchKernelEx(&cfg, quantize_kernel, static_cast<const uint4*>(x), nblocks, g,
+                                        reinterpret_cast<uint2*>(codes), sf));
+  }
+  const int64_t groups = (C + 3) / 4;
+  const int64_t tiles_per_band = (groups + kQPAtoms - 1) / kQPAtoms;
+  const int64_t num_tiles = ((rows + 127) / 128) * tiles_per_band;
+  cudaLaunchConfig_t cfg = programmatic_config(grid_for(num_tiles * kQPThreads, kQPThreads, dev, 4), kQPThreads, stream);
   set_programmatic(cfg, attr);
-  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_kernel, static_cast<const uint4*>(x), nblocks, g,
-                                      reinterpret_cast<uint2*>(codes), sf));
+  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_packed_kernel, static_cast<const uint4*>(x), rows, C, groups,
+                                      tiles_per_band, num_tiles, g, reinterpret_cast<uint2*>(codes),
+                                      reinterpret_cast<uint32_t*>(sf)));
 }
 
 nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out, cudaStream_t stream,

@@ -77,3 +77,37 @@ def test_quantize_then_pack_feeds_gemm_layout():
     _, sf = nv.quantize(dev_bf16(x), g)
     packed = nv.pack_scales(sf, 512).cpu().numpy()
     assert np.array_equal(packed, O.pack_scales(O.quantize(x, g)[1]))
+
+
+@pytest.mark.parametrize("R,K,std", [(1, 16, 1.0), (129, 320, 1.0), (300, 5120, 0.02), (256, 48, 1.0),
+                                     (8192, 5120, 1.0)])
+def test_quantize_packed_byte_exact(R, K, std):
+    # Fused quantize + pack: codes as nvfp4_quantize, scales byte for byte the oracle's
+    # pack of the oracle's row-major scales, zero padding included (ragged rows and
+    # a ragged last atom).
+    x = G.bf16_normal(R, K, 9, "x", std)
+    g = O.global_scale(x)
+    sf_packed = torch.full((nv.packed_scales_bytes(R, K),), 0xAB, dtype=torch.uint8, device="cuda")
+    codes, sfp = nv.quantize_packed(dev_bf16(x), g, sf_packed=sf_packed)
+    wc, ws = O.quantize(x, g)
+    assert np.array_equal(codes.cpu().numpy(), wc)
+    assert np.array_equal(sfp.cpu().numpy(), O.pack_scales(ws))
+
+
+def test_quantize_packed_then_gemm():
+    # The W4A4 prefill chain without a separate pack: quantize_packed on both operands,
+    # then the GEMM, within the tolerance of the oracle on the oracle's own operands.
+    M, N, K = 200, 384, 1024
+    x = G.bf16_normal(M, K, 12, "x")
+    w = G.bf16_normal(N, K, 12, "w", 0.02)
+    gx, gw = O.global_scale(x), O.global_scale(w)
+    A, sfa = nv.quantize_packed(dev_bf16(x), gx)
+    B, sfb = nv.quantize_packed(dev_bf16(w), gw)
+    alpha = float(np.float32(gx) * np.float32(gw))
+    D = nv.gemm(A, sfa, B, sfb, alpha, M, N, K)
+    torch.cuda.synchronize()
+    Ah, SFAh = O.quantize(x, gx)
+    Bh, SFBh = O.quantize(w, gw)
+    ref, abs_sum = O.gemm(Ah, SFAh, Bh, SFBh, alpha)
+    from gpu_util import assert_within, host_f64
+    assert_within(host_f64(D), ref, abs_sum, alpha, "quantize_packed -> gemm")
