@@ -237,9 +237,13 @@ def time_gemm(S, steps, warmup, world, sampler=None):
 
 
 def time_gemm_e2e(S, steps, warmup):
-    """Same GEMM through the C ABI with host buffers: H2D of A, B, SFA, SFB from pinned
-    memory, the GEMM, and D2H of D, all inside the timed region."""
-    import numpy as np
+    """Same GEMM end to end through the C ABI with host buffers: every step copies
+    its A, B, SFA, SFB from pinned host memory to the device, runs the GEMM and
+    copies D back to pinned host memory, all inside the timed region.  Steps are
+    pipelined the way a serving loop would run them: host-to-device copies, GEMMs
+    and device-to-host copies on three streams with two device buffer sets, so step
+    i's result copy-out overlaps step i+1's copy-in and GEMM (stream events order
+    each buffer set's reuse).  Returns (ms per step, h2d bytes, d2h bytes)."""
     import torch
 
     import nvfp4_block_scaled_gb300 as nv
@@ -254,31 +258,54 @@ def time_gemm_e2e(S, steps, warmup):
     hB = torch.from_numpy(B).pin_memory()
     hSFA = sfa_p.pin_memory()
     hSFB = sfb_p.pin_memory()
-    hD = torch.empty((S, S), dtype=torch.bfloat16).pin_memory()
-    dA, dB = torch.empty_like(hA, device="cuda"), torch.empty_like(hB, device="cuda")
-    dSFA, dSFB = torch.empty_like(hSFA, device="cuda"), torch.empty_like(hSFB, device="cuda")
-    dD = torch.empty((S, S), dtype=torch.bfloat16, device="cuda")
+    hD = [torch.empty((S, S), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    bufs = [dict(A=torch.empty_like(hA, device="cuda"), B=torch.empty_like(hB, device="cuda"),
+                 SFA=torch.empty_like(hSFA, device="cuda"), SFB=torch.empty_like(hSFB, device="cuda"),
+                 D=torch.empty((S, S), dtype=torch.bfloat16, device="cuda")) for _ in range(2)]
+    s_in, s_gemm, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    inputs_free = [ev(), ev()]   # the GEMM that read set k has finished
+    inputs_ready = [ev(), ev()]
+    d_ready = [ev(), ev()]
+    d_free = [ev(), ev()]        # set k's D has been copied out
+    used = [False, False]
 
-    def step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        dSFA.copy_(hSFA, non_blocking=True)
-        dSFB.copy_(hSFB, non_blocking=True)
-        nv.gemm(dA, dSFA, dB, dSFB, alpha, S, S, S, out=dD)
-        hD.copy_(dD, non_blocking=True)
+    def step(i):
+        k = i % 2
+        b = bufs[k]
+        with torch.cuda.stream(s_in):
+            if used[k]:
+                s_in.wait_event(inputs_free[k])
+            b["A"].copy_(hA, non_blocking=True)
+            b["B"].copy_(hB, non_blocking=True)
+            b["SFA"].copy_(hSFA, non_blocking=True)
+            b["SFB"].copy_(hSFB, non_blocking=True)
+            inputs_ready[k].record(s_in)
+        with torch.cuda.stream(s_gemm):
+            s_gemm.wait_event(inputs_ready[k])
+            if used[k]:
+                s_gemm.wait_event(d_free[k])
+            nv.gemm(b["A"], b["SFA"], b["B"], b["SFB"], alpha, S, S, S, out=b["D"], stream=s_gemm)
+            inputs_free[k].record(s_gemm)
+            d_ready[k].record(s_gemm)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(d_ready[k])
+            hD[k].copy_(b["D"], non_blocking=True)
+            d_free[k].record(s_out)
+        used[k] = True
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
+    e0.record(s_in)
+    for i in range(steps):
+        step(warmup + i)
+    e1.record(s_out)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     h2d = hA.numel() + hB.numel() + hSFA.numel() + hSFB.numel()
-    d2h = hD.numel() * 2
+    d2h = hD[0].numel() * 2
     return ms, h2d, d2h
 
 
@@ -570,7 +597,7 @@ def run_ours(args):
                               "tflops": round(2 * 16384 ** 3 / (statistics.mean(t16) / 1e3) / 1e12, 1),
                               "frac_of_peak": round(2 * 16384 ** 3 / (statistics.mean(t16) / 1e3) / 1e12 / peak, 4)}
         if rank == 0:
-            ms, h2d, d2h = time_gemm_e2e(S, 5, 2)
+            ms, h2d, d2h = time_gemm_e2e(S, 10, 3)
             line["e2e"] = {"value": round(flops / (ms / 1e3) / 1e12, 1), "unit": "TFLOP/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                            "ms_per_step": round(ms, 3)}
