@@ -391,8 +391,8 @@ def bench_llm(peaks, configs=(0,), shapes=None):
     N(0,0.02) in BF16 (seeded device RNG), quantised by nvfp4_quantize with per-tensor
     scales, scales packed.  Per-call time from CUDA-graph replay of one call per
     rotated weight copy (copies totalling >= 4x L2, so each call reads its weight
-    from HBM).  Each cell reports its roofline bound: max(2MNK / FP4 peak, bytes /
-    HBM bandwidth)."""
+    from HBM), for the automatic configuration and for nvfp4_gemm_streamk.  Each cell
+    reports its roofline bound: max(2MNK / FP4 peak, bytes / HBM bandwidth)."""
     import math
 
     import torch
@@ -427,9 +427,15 @@ def bench_llm(peaks, configs=(0,), shapes=None):
         t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
         cell = {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
                 "roofline_us": round(max(t_tensor, t_hbm), 2), "copies": copies}
-        for cfg in configs:
+        ws = torch.zeros(nv.gemm_streamk_workspace_bytes(), dtype=torch.uint8, device="cuda")
+        for cfg in list(configs) + ["streamk"]:
+            def call(i, stream=None, cfg=cfg):
+                if cfg == "streamk":
+                    nv.gemm_streamk(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, ws, out=D, stream=stream)
+                else:
+                    nv.gemm(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, out=D, config=cfg, stream=stream)
             for i in range(2):
-                nv.gemm(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, out=D, config=cfg)
+                call(i)
             torch.cuda.synchronize()
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
@@ -437,7 +443,7 @@ def bench_llm(peaks, configs=(0,), shapes=None):
             with torch.cuda.stream(s):
                 with torch.cuda.graph(g, stream=s):
                     for i in range(copies):
-                        nv.gemm(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, out=D, config=cfg, stream=s)
+                        call(i, s)
             torch.cuda.current_stream().wait_stream(s)
             g.replay()
             torch.cuda.synchronize()
@@ -451,13 +457,13 @@ def bench_llm(peaks, configs=(0,), shapes=None):
                 us = e0.elapsed_time(e1) * 1e3 / copies
                 best = us if best is None else min(best, us)
             del g
-            key = "auto" if cfg == 0 else f"config{cfg}"
+            key = cfg if cfg == "streamk" else ("auto" if cfg == 0 else f"config{cfg}")
             cell[key] = {"us": round(best, 2), "tflops": round(flops / best / 1e6, 1),
                          "roofline_frac": round(max(t_tensor, t_hbm) / best, 3)}
         if 0 in configs:
             cell["auto_config"] = nv.gemm_config_name(nv.gemm_choose_config(M, N, K)).split(" ")[0]
         out[f"M{M}_N{N}_K{K}"] = cell
-        del A, B, SFA, SFB, sfa, sfb, D, Bs, sfbs
+        del A, B, SFA, SFB, sfa, sfb, D, Bs, sfbs, ws
     err = nv.device_error()
     if err != 0:
         raise RuntimeError(f"device error {err}")

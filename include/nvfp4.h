@@ -158,6 +158,39 @@ nvfp4_status nvfp4_gemm_config(const uint8_t* A, const uint8_t* SFA, const uint8
                                const uint8_t* SFB, float alpha, void* D_bf16, int64_t M,
                                int64_t N, int64_t K, int config, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_gemm_streamk -- nvfp4_gemm with a stream-K schedule for the CTA-pair kernel.
+ *
+ * When the 256x256 output tiles are not a whole number of waves of CTA pairs, the
+ * last one or two waves' (tile, K-block) units are split evenly over the pairs, each
+ * pair taking one contiguous run of them ([P2] Design section, stream-K); a tile
+ * shared by two pairs is finished by the second, which adds the first one's FP32
+ * partial (written to the workspace) in a fixed order, so repeated calls are
+ * bit-identical (not bit-identical to nvfp4_gemm, whose summation order differs).
+ * The split is taken only where a cost model in K-blocks per pair, charging the
+ * fix-up as 8 K-blocks, predicts a gain over the data-parallel waves (measured:
+ * 1024x5120x17408 58 us against 85 us, 1024x5120x5120 31 against 36); otherwise, and
+ * for shapes the pair kernel does not take, the call runs as nvfp4_gemm.
+ *
+ *   A, SFA, B, SFB, alpha, D_bf16, M, N, K   as nvfp4_gemm.
+ *   workspace        DEVICE buffer owned by the caller, at least
+ *                    nvfp4_gemm_streamk_workspace_bytes() bytes, 16-byte aligned, and
+ *                    zero-filled before its first use.  A call that completes without
+ *                    a device error leaves it ready for the next one (its flag words
+ *                    are back to zero).  Calls that share a workspace must not overlap
+ *                    on the device (calls on one stream never do).
+ *   workspace_bytes  its size.
+ * Errors as nvfp4_gemm, plus NVFP4_ERR_INVALID_ARG for a NULL or too small workspace
+ * and NVFP4_ERR_MISALIGNED for a misaligned one.  After NVFP4_ERR_TIMEOUT the
+ * workspace must be zero-filled again.
+ */
+nvfp4_status nvfp4_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                float alpha, void* D_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Workspace bytes nvfp4_gemm_streamk needs on the current device (any shape), 0 on error. */
+size_t nvfp4_gemm_streamk_workspace_bytes(void);
+
 /* Name of a GEMM kernel configuration, or NULL past the last one (config >= 1). */
 const char* nvfp4_gemm_config_name(int config);
 

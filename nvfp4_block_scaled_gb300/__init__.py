@@ -7,7 +7,8 @@ CUDA stream to the C ABI, and raise ``NVFP4Error`` on a non-OK status.  There is
 no CPU fallback: if the shared library has not been built, the first call raises.
 
 Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
-  quantize, quantize_packed, packed_scales_bytes, pack_scales, gemm, gemm_config_name,
+  quantize, quantize_packed, packed_scales_bytes, pack_scales, gemm, gemm_streamk,
+  gemm_streamk_workspace_bytes, gemm_config_name,
   gemm_choose_config, w4a16_prepared_bytes, w4a16_prepare, w4a16_linear,
   w4a16_linear_colscale, device_error.
 """
@@ -22,7 +23,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 #: Every symbol include/nvfp4.h declares.
 ABI_SYMBOLS = (
     "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_quantize_packed", "nvfp4_packed_scales_bytes",
-    "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_config_name",
+    "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_streamk",
+    "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
     "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_device_error",
 )
@@ -60,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_pack_scales": (c_i, [c_p, c_i64, c_i64, c_p, c_p]),
         "nvfp4_gemm": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_gemm_config": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_i, c_p]),
+        "nvfp4_gemm_streamk": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p, ctypes.c_size_t, c_p]),
+        "nvfp4_gemm_streamk_workspace_bytes": (ctypes.c_size_t, []),
         "nvfp4_gemm_config_name": (ctypes.c_char_p, [c_i]),
         "nvfp4_gemm_choose_config": (c_i, [c_i64, c_i64, c_i64]),
         "nvfp4_w4a16_prepared_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
@@ -189,6 +193,26 @@ def gemm(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, out=None, config:
     _check("nvfp4_gemm", lib.nvfp4_gemm_config(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
         int(config), _stream(stream)))
+    return out
+
+
+def gemm_streamk_workspace_bytes() -> int:
+    return int(load_library().nvfp4_gemm_streamk_workspace_bytes())
+
+
+def gemm_streamk(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, workspace, out=None, stream=None):
+    """nvfp4_gemm with the stream-K schedule; workspace: zero-filled uint8 CUDA tensor of at
+    least gemm_streamk_workspace_bytes() bytes, reusable across calls on one stream."""
+    import torch
+
+    for t, nm in ((A, "A"), (SFA, "SFA"), (B, "B"), (SFB, "SFB"), (workspace, "workspace")):
+        _cuda(t, nm, torch.uint8)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("nvfp4_gemm_streamk", load_library().nvfp4_gemm_streamk(
+        _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
+        _ptr(workspace), int(workspace.numel()), _stream(stream)))
     return out
 
 

@@ -242,6 +242,28 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
   return nvfp4_gemm_config(A, SFA, B, SFB, alpha, D_bf16, M, N, K, 0, stream);
 }
 
+size_t nvfp4_gemm_streamk_workspace_bytes(void) {
+  DeviceInfo dev;
+  if (current_device(&dev) != NVFP4_OK) return 0;
+  return gemm_streamk_workspace_bytes(dev);
+}
+
+nvfp4_status nvfp4_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                float alpha, void* D_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, nvfp4_stream_t stream) {
+  nvfp4_status st = gemm_checks(A, SFA, B, SFB, alpha, D_bf16, M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (workspace == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  const size_t need = gemm_streamk_workspace_bytes(dev);
+  if (need == 0) return NVFP4_ERR_CUDA;
+  if (workspace_bytes < need) return NVFP4_ERR_INVALID_ARG;
+  return launch_gemm_streamk(A, SFA, B, SFB, alpha, D_bf16, M, N, K, workspace, as_stream(stream), dev);
+}
+
 const char* nvfp4_gemm_config_name(int config) { return gemm_config_name(config); }
 
 int nvfp4_gemm_choose_config(int64_t M, int64_t N, int64_t K) {

@@ -612,7 +612,7 @@ constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
 constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 4 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
 constexpr int kOffBar = kOffOut + 4 * kOutBox;
-constexpr int kNumBars = 3 * kStages + 2;
+constexpr int kNumBars = 3 * kStages + 4;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
@@ -627,11 +627,81 @@ static_assert(kTmemSF + kStages * kSFSlotCols <= kTmemCols, "TMEM budget");
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(256 >> 3) << 17) |
                             (static_cast<uint32_t>(256 >> 4) << 24);
 
+// Work of one pair, as a list of segments (tile, K-stage range, kind) that every
+// role walks in the same order.
+//   Data-parallel (streamk = 0): tiles pair, pair + P, pair + 2P, ..., all full.
+//   Stream-K (streamk = 1; tiles >= P and not a multiple of P): the first
+//   (tiles / P - 1) waves stay data-parallel (strided tiles keep a wave's operands
+//   together in L2); the remaining R tiles (P <= R < 2P) form R x KB (tile, stage)
+//   units split evenly over the P pairs.  Each pair's range holds at least KB units,
+//   so a tile is shared by at most two pairs: pair p's range may end inside a tile
+//   (its HEAD piece: stages [0, k_end), published to the workspace) and begin inside
+//   the tile whose head pair p - 1 computed (its TAIL piece: stages [k_first, KB),
+//   added to that head partial).  Order: data-parallel tiles, the head piece, the
+//   whole stream-K tiles, the tail piece -- so a head is published long before the
+//   pair that needs it gets there.
+struct PairSched {
+  enum { kFull = 0, kHead = 1, kTail = 2 };
+  int p, P, tiles, KB;
+  int dp;                       // data-parallel tiles of this pair
+  int t_first, k_first, t_last, k_end, tf0, nfull, has_head, has_tail;
+
+  __device__ void init(int p_, int P_, int tiles_, int KB_, int streamk) {
+    p = p_; P = P_; tiles = tiles_; KB = KB_;
+    has_head = has_tail = nfull = 0;
+    tf0 = t_first = t_last = k_first = k_end = 0;
+    if (!streamk) {
+      dp = p < tiles ? (tiles - p + P - 1) / P : 0;
+      return;
+    }
+    dp = tiles / P - 1;
+    const int T0 = dp * P;
+    const int64_t U = static_cast<int64_t>(tiles - T0) * KB;
+    const int64_t u0 = static_cast<int64_t>(p) * U / P, u1 = static_cast<int64_t>(p + 1) * U / P;
+    t_first = T0 + static_cast<int>(u0 / KB);
+    k_first = static_cast<int>(u0 % KB);
+    t_last = T0 + static_cast<int>((u1 - 1) / KB);
+    k_end = static_cast<int>((u1 - 1) % KB) + 1;
+    has_tail = k_first > 0;
+    has_head = k_end < KB;
+    tf0 = has_tail ? t_first + 1 : t_first;
+    const int tf1 = has_head ? t_last - 1 : t_last;
+    nfull = tf1 >= tf0 ? tf1 - tf0 + 1 : 0;
+  }
+  __device__ int count() const { return dp + has_head + nfull + has_tail; }
+  __device__ void seg(int s, int& tile, int& kb0, int& kb1, int& kind) const {
+    if (s < dp) { tile = p + s * P; kb0 = 0; kb1 = KB; kind = kFull; return; }
+    s -= dp;
+    if (has_head) {
+      if (s == 0) { tile = t_last; kb0 = 0; kb1 = k_end; kind = kHead; return; }
+      --s;
+    }
+    if (s < nfull) { tile = tf0 + s; kb0 = 0; kb1 = KB; kind = kFull; return; }
+    tile = t_first; kb0 = k_first; kb1 = KB; kind = kTail;
+  }
+};
+
+// Bounded wait (2 s) for a stream-K flag to read 1 (acquire, GPU scope).
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, volatile int* abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == 1u) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      record_device_error(kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                           const __grid_constant__ CUtensorMap tmD, float alpha, int K, int tiles_m, int tiles_n,
-                          int group_n) {
+                          int group_n, int streamk, float* __restrict__ ws, uint32_t* __restrict__ flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -640,6 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_accf = bar_empty + 8 * kStages;
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_sf = bar_acce + 8;                 // stage's scales are in TMEM (leader)
+  const uint32_t bar_pub = bar_sf + 8 * kStages;        // stream-K: this CTA's head partial is written
+  const uint32_t bar_seen = bar_pub + 8;                // stream-K: the head partial of the tail is ready
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
 
@@ -658,6 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, 2 * kEpiWarps);
     for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, kSFWarps);
+    mbar_init(bar_pub, kEpiWarps);  // each used at most once per launch (phase 0)
+    mbar_init(bar_seen, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -679,6 +753,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = tiles_m * tiles_n;
   const int KB = (K + kBKP - 1) / kBKP;
   const int KG = K / kMmaK;  // scale atoms per 128-row band
+  PairSched sched;
+  sched.init(pair_id, num_pairs, num_tiles, KB, streamk);
+  const int nseg = sched.count();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -696,11 +773,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d_pair(sbase + kOffSFA + st * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
                          mt * 2 + static_cast<int>(rank));
       };
-      for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+      for (int s = 0; s < nseg && ok; ++s) {
+        int t, kb0, kb1, kind;
+        sched.seg(s, t, kb0, kb1, kind);
         int mt, nt;
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int b_row = nt * 256 + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (dfr.full()) dfr.flush(load_a);
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
@@ -730,10 +809,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
+      for (int s = 0; s < nseg && ok; ++s) {
+        int t, kb0, kb1, kind;
+        sched.seg(s, t, kb0, kb1, kind);
         if (!mbar_wait(bar_acce, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           if (!mbar_wait(bar_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -746,7 +827,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t koff = (j >> 2) * kSubTile + (j & 3) * (kMmaK / 2);
             const uint64_t adesc = make_sdesc(sA + koff, 16, 1024, 2);
             const uint64_t bdesc = make_sdesc(sB + koff, 16, 1024, 2);
-            tc_mma_nvf4_pair(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            tc_mma_nvf4_pair(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j,
+                             (kb != kb0 || j != 0) ? 1u : 0u);
           }
           tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -771,8 +853,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = pair_id; t < num_tiles && ok; t += num_pairs) {
-        for (int kb = 0; kb < KB; ++kb) {
+      for (int s = 0; s < nseg && ok; ++s) {
+        int t, kb0, kb1, kind;
+        sched.seg(s, t, kb0, kb1, kind);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nk = min(kStepsP, KG - kb * kStepsP);
@@ -802,11 +886,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;                   // accumulator row = TMEM lane
     uint32_t acc_phase = 0;
     bool stored = false;
-    for (int t = pair_id; t < num_tiles; t += num_pairs) {
+    // Stream-K workspace slots: one 128 KB FP32 partial per (pair, rank) and one flag
+    // each.  A slot is laid out in the epilogue's own register order, [warp][32-column
+    // chunk][float4 i][lane], so that both the publishing and the finishing CTA (same
+    // rank, hence the same TMEM lanes and warp roles) move it with whole 512-byte warp
+    // accesses.
+    const size_t slot_f4 = 128 * 256 / 4;
+    const int ew = warp - kFirstEpiWarp;           // epilogue warp 0..7
+    for (int s = 0; s < nseg; ++s) {
+      int t, kb0, kb1, kind;
+      sched.seg(s, t, kb0, kb1, kind);
       int mt, nt;
       tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
+      const float4* part = nullptr;  // the head pair's partial of this tile (tail piece)
+      float4 hp[8];                  // its current 32-column chunk
+      if (kind == PairSched::kTail) {
+        // While this pair's own MMAs still run: one thread watches the flag, resets it
+        // for the next call (the head pair publishes this slot once per launch) and
+        // releases the other warps, which fetch their first chunk of the partial.
+        uint32_t* flag = flags + (pair_id - 1) * 2 + rank;
+        if (warp == kFirstEpiWarp && lane == 0 && wait_flag(flag, abort_flag)) {
+          asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(0u) : "memory");
+          mbar_arrive(bar_seen);
+        }
+        if (!warp_wait(bar_seen, 0, abort_flag)) break;
+        part = reinterpret_cast<const float4*>(ws) + (static_cast<size_t>(pair_id - 1) * 2 + rank) * slot_f4 +
+               static_cast<size_t>(ew) * (4 * 8 * 32) + lane;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hp[i] = __ldcg(part + i * 32);
+      }
       if (!warp_wait(bar_accf, acc_phase, abort_flag)) break;
       tc_fence_after();
+      if (kind == PairSched::kHead) {
+        // ---- head piece: publish the FP32 partial tile for the pair that finishes it
+        float4* dst = reinterpret_cast<float4*>(ws) + (static_cast<size_t>(pair_id) * 2 + rank) * slot_f4 +
+                      static_cast<size_t>(ew) * (4 * 8 * 32) + lane;
+#pragma unroll 1
+        for (int c32 = 0; c32 < 4; ++c32) {
+          const int col0 = h * 128 + c32 * 32;
+          uint32_t v[32];
+          tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(dst + (c32 * 8 + i) * 32, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                         __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+        }
+        // The accumulator is read out: hand it back before the stores drain.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_leader);
+        __threadfence();  // this warp's stores are visible at GPU scope before its arrival
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pub);
+        if (warp == kFirstEpiWarp && lane == 0 && mbar_wait(bar_pub, 0, abort_flag)) {
+          __threadfence();
+          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + pair_id * 2 + rank), "r"(1u) : "memory");
+        }
+        acc_phase ^= 1;
+        continue;
+      }
       if (stored) {  // the previous tile's stores must have finished reading the staging tile
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
@@ -816,7 +955,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = h * 128 + c32 * 32;
         uint32_t v[32];
         tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
-        tc_wait_ld();
+        if (part != nullptr) {
+          // fixed order: this pair's stages, then the head pair's partial; the next
+          // chunk's loads go out before this one is used
+          float4 hn[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hn[i] = c32 < 3 ? __ldcg(part + ((c32 + 1) * 8 + i) * 32) : hp[i];
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + hp[i].x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + hp[i].y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + hp[i].z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + hp[i].w);
+            hp[i] = hn[i];
+          }
+        } else {
+          tc_wait_ld();
+        }
         const uint32_t box = out_base + (2 * h + (c32 >> 1)) * kOutBox + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -993,15 +1149,15 @@ nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
                                       static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), S));
 }
 
-nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
-                      void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
-  auto kern = pair::gemm_nvf4_pair_kernel;
-  static bool attr_set[64] = {};
+// Pairs that can be co-resident (cudaOccupancyMaxActiveClusters for clusters of
+// two), queried once per device; also sets the kernel's shared-memory limit.
+int pair_slots(const DeviceInfo& dev) {
   static int max_clusters[64] = {};
   const int d = dev.device < 64 ? dev.device : 63;
-  if (!attr_set[d]) {
+  if (max_clusters[d] == 0) {
+    auto kern = pair::gemm_nvf4_pair_kernel;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
+      return -1;
     cudaLaunchConfig_t qc = {};
     qc.gridDim = dim3(dev.num_sms, 1, 1);
     qc.blockDim = dim3(pair::kThreads, 1, 1);
@@ -1016,8 +1172,26 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess || n < 1) n = dev.num_sms / 2;
     max_clusters[d] = n;
-    attr_set[d] = true;
   }
+  return max_clusters[d];
+}
+
+// Stream-K workspace: one flag per (pair, rank), padded to 1 KB, then one 128 x 256
+// FP32 partial tile per (pair, rank).
+constexpr size_t kPartialBytes = 128 * 256 * 4;
+constexpr int64_t kStreamKFixupKB = 8;
+size_t streamk_flags_bytes(int pairs) { return ((static_cast<size_t>(pairs) * 2 * 4 + 1023) / 1024) * 1024; }
+size_t streamk_bytes(int pairs) { return streamk_flags_bytes(pairs) + static_cast<size_t>(pairs) * 2 * kPartialBytes; }
+
+// streamk: run the hybrid data-parallel / stream-K schedule (workspace required) when
+// the tiles are not a whole number of waves; otherwise, or with streamk == false,
+// the data-parallel schedule.
+nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
+                      void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev,
+                      bool streamk = false, void* ws = nullptr) {
+  auto kern = pair::gemm_nvf4_pair_kernel;
+  const int slots = pair_slots(dev);
+  if (slots < 0) return NVFP4_ERR_CUDA;
   CUtensorMap ta, tb, tsfa, tsfb, td;
   // A and B as [K/256 chunks][rows][128 bytes]: one box = 128 rows x one stage's chunks.
   nvfp4_status st = encode_tmap_u8_3d_chunks(&ta, A, M, K, 128, pair::kBKP / 256);
@@ -1032,8 +1206,22 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   const int tiles_m = static_cast<int>((M + 255) / 256);
   const int tiles_n = static_cast<int>((N + 255) / 256);
   const int num_tiles = tiles_m * tiles_n;
-  const int pairs = num_tiles < max_clusters[d] ? num_tiles : max_clusters[d];
+  int use_sk = (streamk && ws != nullptr && num_tiles > slots && num_tiles % slots != 0) ? 1 : 0;
+  if (use_sk) {
+    // Cost per pair in K-blocks: data-parallel waves against whole waves plus an even
+    // share of the rest plus the fix-up (one partial written, one read back; about
+    // four microseconds, eight K-blocks).  Ties stay data-parallel.
+    const int64_t KB = K / pair::kBKP;
+    const int64_t waves = (num_tiles + slots - 1) / slots;
+    const int64_t whole = num_tiles / slots - 1;
+    const int64_t units = (num_tiles - whole * slots) * KB;
+    const int64_t sk_cost = whole * KB + (units + slots - 1) / slots + kStreamKFixupKB;
+    use_sk = sk_cost < waves * KB ? 1 : 0;
+  }
+  const int pairs = use_sk ? slots : (num_tiles < slots ? num_tiles : slots);
   const int group_n = tiles_n < 8 ? tiles_n : 8;
+  uint32_t* flags = use_sk ? static_cast<uint32_t*>(ws) : nullptr;
+  float* part = use_sk ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + streamk_flags_bytes(slots)) : nullptr;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(pair::kThreads, 1, 1);
@@ -1048,7 +1236,7 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, tsfa, tsfb, td, alpha, static_cast<int>(K), tiles_m,
-                                      tiles_n, group_n));
+                                      tiles_n, group_n, use_sk, part, flags));
 }
 
 }  // namespace
@@ -1085,6 +1273,21 @@ int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   if (K % 256 == 0 && M > 128 && N > 128) return 3;
   if (N <= 128 || tiles256 < dev.num_sms / 2) return 2;
   return 1;
+}
+
+size_t gemm_streamk_workspace_bytes(const DeviceInfo& dev) {
+  const int slots = pair_slots(dev);
+  return slots > 0 ? streamk_bytes(slots) : 0;
+}
+
+nvfp4_status launch_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                 float alpha, void* D, int64_t M, int64_t N, int64_t K, void* ws,
+                                 cudaStream_t stream, const DeviceInfo& dev) {
+  // The stream-K schedule belongs to the CTA-pair kernel; shapes that do not run it
+  // take the automatic configuration (and leave the workspace untouched).
+  const int config = gemm_choose_config(M, N, K, dev);
+  if (config != 3 || K % 256 != 0) return launch_gemm(config, A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+  return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, true, ws);
 }
 
 nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,

@@ -76,6 +76,13 @@ nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const
                          const uint8_t* SFB, float alpha, void* D, int64_t M, int64_t N, int64_t K,
                          cudaStream_t stream, const DeviceInfo& dev);
 
+// Stream-K GEMM: workspace bytes for the current device, and the launch (falls back
+// to launch_gemm's automatic configuration for shapes the CTA-pair kernel does not take).
+size_t gemm_streamk_workspace_bytes(const DeviceInfo& dev);
+nvfp4_status launch_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                 float alpha, void* D, int64_t M, int64_t N, int64_t K, void* ws,
+                                 cudaStream_t stream, const DeviceInfo& dev);
+
 nvfp4_status launch_w4a16_prepare(const uint8_t* W, const uint8_t* SW, int64_t N, int64_t K, void* Wprep,
                                   cudaStream_t stream, const DeviceInfo& dev);
 // alpha_col: NULL for the global scale alpha, else N per-output-column FP32 scales.

@@ -254,3 +254,105 @@ def test_gemm_back_to_back_writes_keep_the_last(M, N, K):
         nv.gemm(a2, sfa2, b, sfb, 1.0, M, N, K, out=D)
     torch.cuda.synchronize()
     assert torch.equal(D.view(torch.int16), want.view(torch.int16))
+
+
+def _streamk_workspace():
+    return torch.zeros(nv.gemm_streamk_workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+
+def _partials_written(ws):
+    # the flag words take the first KB; the FP32 partial tiles follow
+    return bool(ws[1024:].any())
+
+
+@pytest.mark.parametrize("M,N,K", [(2304, 2304, 4096), (2200, 2104, 4096), (2304, 4864, 4096)])
+def test_gemm_streamk_full(M, N, K):
+    # 81 / 81 / 171 tiles of 256 x 256 on about 76 CTA pairs, 16 K-blocks each: the last
+    # waves' (tile, K-block) units are split over the pairs, and tiles shared by two pairs
+    # are finished from a partial in the workspace (ragged edges in the second shape).
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=M + K, scales="zero_sub")
+    alpha = G.alpha_uniform(K)
+    ws = _streamk_workspace()
+    sfa, sfb, a, b = nv.pack_scales(dev(SFA), K), nv.pack_scales(dev(SFB), K), dev(A), dev(B)
+    D = nv.gemm_streamk(a, sfa, b, sfb, alpha, M, N, K, ws)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert _partials_written(ws), "the stream-K schedule did not run"
+    check_full(A, SFA, B, SFB, alpha, D, f"stream-K {M}x{N}x{K}")
+    # the workspace is ready for the next call: same bits again, flags back to zero
+    for _ in range(3):
+        D2 = nv.gemm_streamk(a, sfa, b, sfb, alpha, M, N, K, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
+    flags = ws[:1024].view(torch.int32)
+    assert int(flags.abs().sum()) == 0
+
+
+def test_gemm_streamk_all_scales_one_is_bit_exact():
+    M, N, K = 2304, 2304, 3072
+    A = G.packed_codes_uniform(M, K, 1, "A")
+    B = G.packed_codes_uniform(N, K, 1, "B")
+    S1 = np.full((M, K // 16), 0x38, np.uint8)
+    S2 = np.full((N, K // 16), 0x38, np.uint8)
+    ws = _streamk_workspace()
+    D = nv.gemm_streamk(dev(A), nv.pack_scales(dev(S1), K), dev(B), nv.pack_scales(dev(S2), K), 1.0, M, N, K, ws)
+    torch.cuda.synchronize()
+    assert _partials_written(ws)
+    exact = O.gemm_exact_units(A, S1, B, S2).astype(np.float64) * 2.0 ** -20
+    assert np.array_equal(host_bits(D), O.f32_to_bf16_rne(exact.astype(np.float32)))
+
+
+def test_gemm_streamk_llm_layer_and_graph_replay():
+    # 1024 tokens x (5120, 5120): 80 tiles for ~76 pairs, the case stream-K is for.
+    M, N, K = 1024, 5120, 5120
+    x = G.bf16_normal(M, K, 13, "x")
+    w = G.bf16_normal(N, K, 13, "w", 0.02)
+    gx, gw = O.global_scale(x), O.global_scale(w)
+    alpha = float(np.float32(gx) * np.float32(gw))
+    A, sfa = nv.quantize_packed(dev_bf16(x), gx)
+    B, sfb = nv.quantize_packed(dev_bf16(w), gw)
+    ws = _streamk_workspace()
+    D = nv.gemm_streamk(A, sfa, B, sfb, alpha, M, N, K, ws)
+    torch.cuda.synchronize()
+    Ah, SFAh = O.quantize(x, gx)
+    Bh, SFBh = O.quantize(w, gw)
+    check_sampled(Ah, SFAh, Bh, SFBh, alpha, D, M, N, 1024, "stream-K llm 1024x5120x5120")
+    out = torch.empty_like(D)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            nv.gemm_streamk(A, sfa, B, sfb, alpha, M, N, K, ws, out=out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert torch.equal(out.view(torch.int16), D.view(torch.int16))
+
+
+def test_gemm_streamk_declined_runs_data_parallel():
+    # 81 tiles but only 4 K-blocks each: the fix-up would cost more than the second wave
+    # it saves, so the call runs the data-parallel pair kernel: nvfp4_gemm's bits, and
+    # the workspace's partial tiles stay untouched.
+    M, N, K = 2304, 2304, 1024
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=21)
+    a, b, sfa, sfb = dev(A), dev(B), nv.pack_scales(dev(SFA), K), nv.pack_scales(dev(SFB), K)
+    ws = _streamk_workspace()
+    D = nv.gemm_streamk(a, sfa, b, sfb, 0.5, M, N, K, ws)
+    want = nv.gemm(a, sfa, b, sfb, 0.5, M, N, K)
+    torch.cuda.synchronize()
+    assert not _partials_written(ws)
+    assert torch.equal(D.view(torch.int16), want.view(torch.int16))
+
+
+def test_gemm_streamk_rejects_bad_workspace():
+    M = N = K = 512
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=3)
+    a, b, sfa, sfb = dev(A), dev(B), nv.pack_scales(dev(SFA), K), nv.pack_scales(dev(SFB), K)
+    small = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.gemm_streamk(a, sfa, b, sfb, 1.0, M, N, K, small)
+    assert e.value.status == -1
