@@ -191,6 +191,37 @@ nvfp4_status nvfp4_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uint
 /* Workspace bytes nvfp4_gemm_streamk needs on the current device (any shape), 0 on error. */
 size_t nvfp4_gemm_streamk_workspace_bytes(void);
 
+/*
+ * nvfp4_gemm_streamk_noalloc -- nvfp4_gemm_streamk with the workspace held inside the
+ * library: a static device array of 20 MiB + 4 KiB per device (flag words plus one
+ * 128 KB FP32 partial per CTA of up to 80 CTA pairs).  Neither cited page has a
+ * counterpart; it is a library convenience, not part of the method.
+ *
+ * It is for callers that cannot hand over a device buffer: code with no allocator
+ * of its own (a plugin or callback inside a host framework that owns the memory
+ * pools), and paths that must not call cudaMalloc/cudaFree because those
+ * synchronise the device or because device memory is fully committed.  The call
+ * allocates nothing: the array's address is looked up once per device
+ * (cudaGetSymbolAddress), and the array comes with the library's module.
+ *
+ *   A, SFA, B, SFB, alpha, D_bf16, M, N, K, stream   as nvfp4_gemm_streamk, whose
+ *                    argument checks, schedule and results (bit for bit) it shares.
+ *   reset_scratch    nonzero: zero the array on `stream` before the launch.  The
+ *                    first call on each device does this by itself; pass it after a
+ *                    call that ended in NVFP4_ERR_TIMEOUT (nvfp4_device_error), which
+ *                    can leave flag words raised.
+ *
+ * There is one array per device, shared by every call on it: calls that overlap on
+ * the GPU (other streams, other host threads) race on it and give wrong results or
+ * time out.  Calls on one stream never overlap.
+ * Errors as nvfp4_gemm_streamk, plus NVFP4_ERR_UNSUPPORTED_DEVICE, before anything is
+ * enqueued, when the device's CTA-pair grid needs more workspace than the array holds,
+ * and NVFP4_ERR_CUDA when the array's address cannot be looked up.
+ */
+nvfp4_status nvfp4_gemm_streamk_noalloc(const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
+                                        const uint8_t* SFB, float alpha, void* D_bf16, int64_t M, int64_t N,
+                                        int64_t K, int reset_scratch, nvfp4_stream_t stream);
+
 /* Name of a GEMM kernel configuration, or NULL past the last one (config >= 1). */
 const char* nvfp4_gemm_config_name(int config);
 

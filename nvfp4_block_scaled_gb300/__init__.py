@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 ABI_SYMBOLS = (
     "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_quantize_packed", "nvfp4_packed_scales_bytes",
     "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_streamk",
-    "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_config_name",
+    "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_streamk_noalloc", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
     "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_device_error",
 )
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_gemm_config": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_i, c_p]),
         "nvfp4_gemm_streamk": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p, ctypes.c_size_t, c_p]),
         "nvfp4_gemm_streamk_workspace_bytes": (ctypes.c_size_t, []),
+        "nvfp4_gemm_streamk_noalloc": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_i, c_p]),
         "nvfp4_gemm_config_name": (ctypes.c_char_p, [c_i]),
         "nvfp4_gemm_choose_config": (c_i, [c_i64, c_i64, c_i64]),
         "nvfp4_w4a16_prepared_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
@@ -213,6 +214,23 @@ def gemm_streamk(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, workspace
     _check("nvfp4_gemm_streamk", load_library().nvfp4_gemm_streamk(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
         _ptr(workspace), int(workspace.numel()), _stream(stream)))
+    return out
+
+
+def gemm_streamk_noalloc(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, out=None, stream=None,
+                         reset_scratch: bool = False):
+    """gemm_streamk with the library's static per-device workspace (no buffer passed, nothing
+    allocated); calls overlapping on the GPU share that workspace and race."""
+    import torch
+
+    for t, nm in ((A, "A"), (SFA, "SFA"), (B, "B"), (SFB, "SFB")):
+        _cuda(t, nm, torch.uint8)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("nvfp4_gemm_streamk_noalloc", load_library().nvfp4_gemm_streamk_noalloc(
+        _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
+        1 if reset_scratch else 0, _stream(stream)))
     return out
 
 
