@@ -629,8 +629,8 @@ constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(256 
 
 // Work of one pair, as a list of segments (tile, K-stage range, kind) that every
 // role walks in the same order.
-//   Data-parallel (streamk = 0): tiles pair, pair + P, pair + 2P, ..., all full.
-//   Stream-K (streamk = 1; tiles >= P and not a multiple of P): the first
+//   Data-parallel (SK = false): tiles pair, pair + P, pair + 2P, ..., all full.
+//   Stream-K (SK = true; tiles >= P and not a multiple of P): the first
 //   (tiles / P - 1) waves stay data-parallel (strided tiles keep a wave's operands
 //   together in L2); the remaining R tiles (P <= R < 2P) form R x KB (tile, stage)
 //   units split evenly over the P pairs.  Each pair's range holds at least KB units,
@@ -669,8 +669,9 @@ struct PairSched {
     nfull = tf1 >= tf0 ? tf1 - tf0 + 1 : 0;
   }
   __device__ int count() const { return dp + has_head + nfull + has_tail; }
+  template <bool SK>
   __device__ void seg(int s, int& tile, int& kb0, int& kb1, int& kind) const {
-    if (s < dp) { tile = p + s * P; kb0 = 0; kb1 = KB; kind = kFull; return; }
+    if (!SK || s < dp) { tile = p + s * P; kb0 = 0; kb1 = KB; kind = kFull; return; }
     s -= dp;
     if (has_head) {
       if (s == 0) { tile = t_last; kb0 = 0; kb1 = k_end; kind = kHead; return; }
@@ -697,11 +698,14 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, volatile int* ab
   }
 }
 
+// SK: the stream-K schedule is compiled in (the data-parallel instantiation carries
+// none of its code or registers).
+template <bool SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                           const __grid_constant__ CUtensorMap tmD, float alpha, int K, int tiles_m, int tiles_n,
-                          int group_n, int streamk, float* __restrict__ ws, uint32_t* __restrict__ flags) {
+                          int group_n, float* __restrict__ ws, uint32_t* __restrict__ flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -754,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = (K + kBKP - 1) / kBKP;
   const int KG = K / kMmaK;  // scale atoms per 128-row band
   PairSched sched;
-  sched.init(pair_id, num_pairs, num_tiles, KB, streamk);
+  sched.init(pair_id, num_pairs, num_tiles, KB, SK ? 1 : 0);
   const int nseg = sched.count();
 
   if (warp == 0) {
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.seg(s, t, kb0, kb1, kind);
+        sched.template seg<SK>(s, t, kb0, kb1, kind);
         int mt, nt;
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int b_row = nt * 256 + static_cast<int>(rank) * 128;
@@ -811,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.seg(s, t, kb0, kb1, kind);
+        sched.template seg<SK>(s, t, kb0, kb1, kind);
         if (!mbar_wait(bar_acce, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -855,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.seg(s, t, kb0, kb1, kind);
+        sched.template seg<SK>(s, t, kb0, kb1, kind);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -895,12 +899,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - kFirstEpiWarp;           // epilogue warp 0..7
     for (int s = 0; s < nseg; ++s) {
       int t, kb0, kb1, kind;
-      sched.seg(s, t, kb0, kb1, kind);
+      sched.template seg<SK>(s, t, kb0, kb1, kind);
       int mt, nt;
       tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
       const float4* part = nullptr;  // the head pair's partial of this tile (tail piece)
       float4 hp[8];                  // its current 32-column chunk
-      if (kind == PairSched::kTail) {
+      if (SK && kind == PairSched::kTail) {
         // While this pair's own MMAs still run: one thread watches the flag, resets it
         // for the next call (the head pair publishes this slot once per launch) and
         // releases the other warps, which fetch their first chunk of the partial.
@@ -917,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!warp_wait(bar_accf, acc_phase, abort_flag)) break;
       tc_fence_after();
-      if (kind == PairSched::kHead) {
+      if (SK && kind == PairSched::kHead) {
         // ---- head piece: publish the FP32 partial tile for the pair that finishes it
         float4* dst = reinterpret_cast<float4*>(ws) + (static_cast<size_t>(pair_id) * 2 + rank) * slot_f4 +
                       static_cast<size_t>(ew) * (4 * 8 * 32) + lane;
@@ -1155,8 +1159,10 @@ int pair_slots(const DeviceInfo& dev) {
   static int max_clusters[64] = {};
   const int d = dev.device < 64 ? dev.device : 63;
   if (max_clusters[d] == 0) {
-    auto kern = pair::gemm_nvf4_pair_kernel;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess)
+    auto kern = pair::gemm_nvf4_pair_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(pair::gemm_nvf4_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair::kSmemBytes) != cudaSuccess)
       return -1;
     cudaLaunchConfig_t qc = {};
     qc.gridDim = dim3(dev.num_sms, 1, 1);
@@ -1189,7 +1195,6 @@ size_t streamk_bytes(int pairs) { return streamk_flags_bytes(pairs) + static_cas
 nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
                       void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev,
                       bool streamk = false, void* ws = nullptr) {
-  auto kern = pair::gemm_nvf4_pair_kernel;
   const int slots = pair_slots(dev);
   if (slots < 0) return NVFP4_ERR_CUDA;
   CUtensorMap ta, tb, tsfa, tsfb, td;
@@ -1235,8 +1240,9 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   set_programmatic(attr[1]);
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  auto kern = use_sk ? pair::gemm_nvf4_pair_kernel<true> : pair::gemm_nvf4_pair_kernel<false>;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, tsfa, tsfb, td, alpha, static_cast<int>(K), tiles_m,
-                                      tiles_n, group_n, use_sk, part, flags));
+                                      tiles_n, group_n, part, flags));
 }
 
 }  // namespace
