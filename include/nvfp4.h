@@ -276,7 +276,7 @@ nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alp
  *
  *     y[m, n] = bf16(alpha_col[n] * sum_k x[m, k] * dequant(W)[n, k]),  FP32 accumulation.
  *
- * [P2] Design: the weight carries "global or per-column scale".  Same kernels,
+ * [P2] Design: the weight scale may be global or per output column.  Same kernels,
  * arguments and rules as nvfp4_w4a16_linear, except:
  *   alpha_col  [N] FP32, DEVICE pointer owned by the caller, 16-byte aligned; read
  *              once per output element (finite values assumed, not checked).
