@@ -18,7 +18,8 @@
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller; the library
- *     allocates no device memory and keeps no per-call state on the device.
+ *     allocates no device memory and keeps no per-call state on the device, except
+ *     for the static workspace array of nvfp4_gemm_streamk_noalloc.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronises the host.  Calls on different streams may run
  *     concurrently.
@@ -73,8 +74,8 @@ int nvfp4_version(void);
 /*
  * nvfp4_quantize -- BF16 activations/weights -> NVFP4 codes + row-major E4M3 scales.
  *
- * The pages name the format ([P2] Design: "packed E2M1, E4M3/UE4M3 block scales,
- * global or per-column scale") but print no quantiser; this is the two-level
+ * The pages name the format ([P2] Design: E2M1 codes packed two per byte, unsigned
+ * E4M3 block scales, a per-tensor or per-column scale) but print no quantiser; this is the two-level
  * NVFP4 recipe, with every step in IEEE float32, round to nearest even, unfused:
  *   s      = E4M3_satfinite( (amax_block / 6) / global_scale )
  *   code_k = E2M1_satfinite( x_k / (dec(s) * global_scale) )
@@ -230,14 +231,14 @@ int nvfp4_gemm_choose_config(int64_t M, int64_t N, int64_t K);
 
 /*
  * Size in bytes of a prepared W4A16 weight: N*K/2 + N*K/16, the size of the
- * checkpoint tensors ([P2] Design, "Weight layout").  0 for invalid N, K.
+ * checkpoint tensors ([P2] Design, weight-layout paragraph).  0 for invalid N, K.
  */
 size_t nvfp4_w4a16_prepared_bytes(int64_t N, int64_t K);
 
 /*
  * nvfp4_w4a16_prepare -- re-lay out an NVFP4 weight once for nvfp4_w4a16_linear.
  *
- * [P2] Design, "Weight layout": codes are moved into the fragment order of the
+ * [P2] Design, weight-layout paragraph: codes are moved into the fragment order of the
  * decode kernel, each E4M3 scale is re-encoded as a byte b with
  * bf16(0x7000 | b<<4) == |scale| * 2^119 (exact for every finite E4M3, subnormals
  * included), zero scales zero their codes and negative scales flip their codes'

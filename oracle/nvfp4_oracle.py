@@ -16,7 +16,8 @@ Sources (cited by page title and section):
 Number formats (E2M1 codes, one E4M3 scale per 16 K-elements, FP32 per-tensor
 alpha): [P1] Version 2 (input footprint: 4 bits per element, 8 bits per 16
 elements) and Version 5 (one scale broadcast to the 16 elements of a micro-block);
-[P2] Design ("packed E2M1, E4M3/UE4M3 block scales, global or per-column scale").
+[P2] Design (two E2M1 codes per byte, one unsigned E4M3 scale per block, and a
+weight scale that is per tensor or per output column).
 
 Everything is computed in float64 (exact for the W4A4 workloads: each product is
 an integer multiple of 2^-20, see ``gemm_exact_units``).  Where the pages fix
@@ -326,7 +327,7 @@ def w4a16_linear(x_bf16_bits, W, SW, alpha: float):
 
 
 def w4a16_linear_colscale(x_bf16_bits, W, SW, alpha_col):
-    """Per-column weight scale ([P2] Design: "global or per-column scale"):
+    """Per-column weight scale ([P2] Design: one weight scale per output column):
     y[m, n] = alpha_col[n] * sum_k x[m, k] * w[n, k].  Returns (ref, scaled_abs_sum),
     float64 [M, N], where scaled_abs_sum[m, n] = |alpha_col[n]| * sum_k |x w|, so
     that ``tolerance(ref, scaled_abs_sum, 1.0)`` is the per-element bound."""
@@ -348,7 +349,7 @@ def w4a16_linear_at(x_bf16_bits, W, SW, alpha: float, rows, cols):
 
 
 # ---------------------------------------------------------------------------
-# W4A16 prepared-weight format ("Wprep").  [P2] Design, "Weight layout": the
+# W4A16 prepared-weight format ("Wprep").  [P2] Design, weight-layout paragraph: the
 # weight is re-laid out once into fragment order, E2M1 codes placed so that
 # shifts and masks give bfloat16 values fp4 * 2^-126, scales re-encoded as a
 # byte b with bf16(0x7000 | b << 4) == scale * 2^119, zero scales zeroing their
