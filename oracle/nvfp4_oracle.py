@@ -95,8 +95,7 @@ def pack_codes(codes: np.ndarray) -> np.ndarray:
 def dequantize(packed: np.ndarray, sf_rowmajor: np.ndarray) -> np.ndarray:
     """float64 [R, K]: element value code * scale, scale = SF[r, k // 16].
 
-    [P1] Version 5: "a single scale-factor ... to the 16 elements of an NVFP4
-    micro-block".
+    [P1] Version 5: one scale factor applies to all 16 elements of a micro-block.
     """
     codes = unpack_codes(packed)
     R, K = codes.shape
@@ -261,7 +260,12 @@ def global_scale(x_bf16_bits) -> float:
 
 def quantize(x_bf16_bits, g: float):
     """bf16 [R, K] (uint16 bits) -> (packed codes [R, K/2] uint8, scales [R, K/16] uint8)."""
-    x = bf16_bits_to_f32(x_bf16_bits)
+    return quantize_f32(bf16_bits_to_f32(x_bf16_bits), g)
+
+
+def quantize_f32(x, g: float):
+    """The quantiser's steps on float32 input [R, K] (bf16 input converts exactly)."""
+    x = np.asarray(x, dtype=np.float32)
     R, K = x.shape
     assert K % 16 == 0
     g32 = np.float32(g)
@@ -276,6 +280,77 @@ def quantize(x_bf16_bits, g: float):
     codes = e2m1_encode_rne_sat(v)
     codes = np.where((sbyte == 0)[:, :, None], np.uint8(0), codes)
     return pack_codes(codes.reshape(R, K)), sbyte
+
+
+# ---------------------------------------------------------------------------
+# Two-pass (value + residual) activation quantisation, [P2] follow-ups: the
+# activations are quantised in two NVFP4 passes, a value pass and a pass over
+# what it left out, and both run on the block-scaled FP4 MMA.  The pages give no
+# formula; the plainest reading, used here:
+#   q1 = quantize(x, g)
+#   r  = x - dequant_f32(q1, g)      (float32: (code * scale) exact, * g RN, x - . RN)
+#   q2 = quantize(r, g)              (same global scale, so one alpha = g * g_w)
+#   D  = alpha * sum_k (dq1_k + dq2_k) * w_k
+# ---------------------------------------------------------------------------
+
+
+def residual_f32(x_bf16_bits, codes1, sf1, g: float) -> np.ndarray:
+    """float32 [R, K]: x - (code * scale) * g, each step an IEEE float32 operation."""
+    x = bf16_bits_to_f32(x_bf16_bits)
+    R, K = x.shape
+    vals = _E2M1[unpack_codes(codes1)].astype(np.float32)
+    scl = np.repeat(_E4M3[np.asarray(sf1, dtype=np.uint8)].astype(np.float32), 16, axis=1)
+    prod = (vals * scl).astype(np.float32)              # exact: at most 5 significant bits
+    dq = (prod * np.float32(g)).astype(np.float32)       # RN multiply
+    return (x - dq).astype(np.float32)                   # RN subtraction
+
+
+def quantize_two_pass(x_bf16_bits, g: float):
+    """bf16 [R, K] -> (codes1, sf1, codes2, sf2): the value pass and the residual pass."""
+    codes1, sf1 = quantize(x_bf16_bits, g)
+    codes2, sf2 = quantize_f32(residual_f32(x_bf16_bits, codes1, sf1, g), g)
+    return codes1, sf1, codes2, sf2
+
+
+def interleave_two_pass(codes1, sf1, codes2, sf2):
+    """The library's two-pass operand: per 256-element K-block j, the value codes of
+    the block then the residual codes of the same block, so a row holds 2K codes.
+
+    Returns (codes [R, K] uint8, scales [R, 2K/16] uint8), row-major; K % 256 == 0.
+    Value byte 128*j + t lands at byte 256*j + t, residual byte 128*j + t at
+    256*j + 128 + t; value scale 16*j + u at 32*j + u, residual at 32*j + 16 + u.
+    """
+    c1, c2 = np.asarray(codes1, np.uint8), np.asarray(codes2, np.uint8)
+    s1, s2 = np.asarray(sf1, np.uint8), np.asarray(sf2, np.uint8)
+    R, half = c1.shape
+    assert (2 * half) % 256 == 0
+    nb = 2 * half // 256
+    codes = np.stack([c1.reshape(R, nb, 128), c2.reshape(R, nb, 128)], axis=2).reshape(R, 2 * half)
+    scales = np.stack([s1.reshape(R, nb, 16), s2.reshape(R, nb, 16)], axis=2).reshape(R, 4 * half // 16)
+    return codes, scales
+
+
+def gemm_two_pass(codes1, sf1, codes2, sf2, B, SFB, alpha: float):
+    """(ref, abs_sum) float64 [M, N] of D = alpha * (dq1 + dq2) w^T.
+
+    abs_sum = sum_k (|dq1_k| + |dq2_k|) |w_k|: both passes' products are summed.
+    """
+    a1 = dequantize(codes1, sf1)
+    a2 = dequantize(codes2, sf2)
+    b = dequantize(B, SFB)
+    ref = ((a1 + a2) @ b.T) * float(alpha)
+    abs_sum = (np.abs(a1) + np.abs(a2)) @ np.abs(b).T
+    return ref, abs_sum
+
+
+def gemm_two_pass_at(codes1, sf1, codes2, sf2, B, SFB, alpha: float, rows, cols):
+    """gemm_two_pass at the sampled outputs (rows[i], cols[i]); float64 [n] each."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    a1 = dequantize(codes1[rows], sf1[rows])
+    a2 = dequantize(codes2[rows], sf2[rows])
+    b = dequantize(B[cols], SFB[cols])
+    return ((a1 + a2) * b).sum(axis=1) * float(alpha), ((np.abs(a1) + np.abs(a2)) * np.abs(b)).sum(axis=1)
 
 
 # ---------------------------------------------------------------------------

@@ -396,3 +396,107 @@ def test_w4a16_colscale_equals_exact_rational_brute_force():
     r1, a1 = O.w4a16_linear_colscale(x, W, SW, np.full(N, 0.5, np.float32))
     r2, a2 = O.w4a16_linear(x, W, SW, 0.5)
     assert np.array_equal(r1, r2) and np.array_equal(a1 * 1.0, a2 * 0.5)
+
+
+# ---------------------------------------------------------------- two-pass (value + residual)
+
+def _bf16_bits_of(values):
+    """Exactly representable values -> bfloat16 bit patterns (float32 bits >> 16)."""
+    f = np.asarray(values, dtype=np.float32)
+    bits = f.view(np.uint32)
+    assert np.all(bits & 0xFFFF == 0), "value not exact in bfloat16"
+    return (bits >> 16).astype(np.uint16)
+
+
+def test_two_pass_hand_worked_block():
+    # tests/golden/two_pass_block.txt: value grid at scale 1, residual grid at 2^-4.
+    rows = _golden_rows("two_pass_block.txt")
+    x = _bf16_bits_of([[float(r[1]) for r in rows]])
+    code1 = [int(r[2], 16) for r in rows]
+    code2 = [int(r[3], 16) for r in rows]
+    c1, s1, c2, s2 = O.quantize_two_pass(x, 1.0)
+    assert s1.tolist() == [[0x38]] and s2.tolist() == [[0x18]]
+    assert O.unpack_codes(c1).tolist() == [code1]
+    assert O.unpack_codes(c2).tolist() == [code2]
+    # the two passes rebuild x exactly
+    rebuilt = O.dequantize(c1, s1) + O.dequantize(c2, s2)
+    assert np.array_equal(rebuilt, O.bf16_bits_to_f64(x))
+
+
+def test_two_pass_of_a_representable_input_has_an_empty_residual():
+    # x = code * scale with the code 6 (byte 7) in every block: the value pass
+    # reproduces codes and scales, the residual is zero, the residual pass all zeros.
+    rng = np.random.default_rng(11)
+    R, K = 8, 64
+    codes = rng.integers(0, 16, size=(R, K))
+    codes[codes == 8] = 0                   # no negative zero in the input
+    codes[:, ::16] = 7                      # a +6 in every block sets its amax
+    sf = rng.integers(0x18, 0x59, size=(R, K // 16)).astype(np.uint8)
+    x = O.dequantize(O.pack_codes(codes.astype(np.uint8)), sf)
+    c1, s1, c2, s2 = O.quantize_two_pass(_bf16_bits_of(x), 1.0)
+    assert np.array_equal(O.unpack_codes(c1), codes) and np.array_equal(s1, sf)
+    assert not c2.any() and not s2.any()
+
+
+def test_two_pass_error_is_within_the_residual_grid_and_far_below_one_pass():
+    # Per element |x - g (dq1 + dq2)| <= dec(s2) g + 6 g 2^-10 + 2^-20 |x|: half of the
+    # widest E2M1 gap (1 scale unit) covers every unsaturated element; a saturated one
+    # misses by at most 6 g times the scale's rounding (0.375 units for normal scales,
+    # 2^-10 absolute for subnormal ones); the float32 steps add a relative 2^-20.
+    x = G.bf16_normal(64, 1024, 5, "x")
+    g = O.global_scale(x)
+    c1, s1, c2, s2 = O.quantize_two_pass(x, g)
+    xf = O.bf16_bits_to_f64(x)
+    err2 = np.abs(xf - (O.dequantize(c1, s1) + O.dequantize(c2, s2)) * g)
+    dec2 = np.repeat(O.e4m3_table()[s2], 16, axis=1)
+    assert np.all(err2 <= dec2 * g + 6 * g * 2.0 ** -10 + 2.0 ** -20 * np.abs(xf))
+    err1 = np.abs(xf - O.dequantize(c1, s1) * g)
+    assert np.sqrt((err2 ** 2).mean()) < np.sqrt((err1 ** 2).mean()) / 4
+
+
+def test_interleave_two_pass_places_blocks_by_hand_offsets():
+    R, K = 2, 512
+    c1 = (np.arange(R * K // 2).reshape(R, K // 2) % 251).astype(np.uint8)
+    c2 = (250 - c1).astype(np.uint8)
+    s1 = (np.arange(R * K // 16).reshape(R, K // 16) % 97).astype(np.uint8)
+    s2 = (s1 + 100).astype(np.uint8)
+    A, S = O.interleave_two_pass(c1, s1, c2, s2)
+    assert A.shape == (2, 512) and S.shape == (2, 64)
+    assert A[0, 0] == c1[0, 0] and A[0, 127] == c1[0, 127]
+    assert A[0, 128] == c2[0, 0] and A[0, 133] == c2[0, 5]
+    assert A[0, 258] == c1[0, 130] and A[1, 511] == c2[1, 255]
+    assert S[0, 15] == s1[0, 15] and S[0, 16] == s2[0, 0]
+    assert S[0, 33] == s1[0, 17] and S[1, 63] == s2[1, 31]
+
+
+def test_gemm_two_pass_equals_exact_rational_brute_force():
+    M, N, K = 2, 3, 256
+    x = G.bf16_normal(M, K, 3, "x")
+    c1, s1, c2, s2 = O.quantize_two_pass(x, O.global_scale(x))
+    B = G.packed_codes_uniform(N, K, 3, "B")
+    SFB = G.scales_uniform_normal(N, K, 3, "SFB")
+    ref, abs_sum = O.gemm_two_pass(c1, s1, c2, s2, B, SFB, 0.75)
+    a1, a2, w = _frac_dequant(c1, s1), _frac_dequant(c2, s2), _frac_dequant(B, SFB)
+    for m in range(M):
+        for n in range(N):
+            s = sum((a1[m][k] + a2[m][k]) * w[n][k] for k in range(K)) * Fraction(3, 4)
+            sa = sum((abs(a1[m][k]) + abs(a2[m][k])) * abs(w[n][k]) for k in range(K))
+            assert Fraction(ref[m, n]) == s          # every term is a multiple of 2^-20
+            assert Fraction(abs_sum[m, n]) == sa
+
+
+def test_gemm_two_pass_is_a_plain_gemm_over_the_interleaved_operand():
+    # The layout the library's kernels run: 2K interleaved activation codes against
+    # the weight with each of its 256-element K-blocks used twice.
+    M, N, K = 5, 7, 512
+    x = G.bf16_normal(M, K, 4, "x")
+    c1, s1, c2, s2 = O.quantize_two_pass(x, O.global_scale(x))
+    B = G.packed_codes_uniform(N, K, 4, "B")
+    SFB = G.scales_uniform_normal(N, K, 4, "SFB")
+    A2, S2 = O.interleave_two_pass(c1, s1, c2, s2)
+    Bd, Sd = O.interleave_two_pass(B, SFB, B, SFB)
+    r1, a1 = O.gemm_two_pass(c1, s1, c2, s2, B, SFB, 1.25)
+    r2, a2 = O.gemm(A2, S2, Bd, Sd, 1.25)
+    assert np.array_equal(r1, r2) and np.array_equal(a1, a2)
+    r3, _ = O.gemm_two_pass_at(c1, s1, c2, s2, B, SFB, 1.25, [4, 0], [6, 2])
+    assert np.array_equal(r3, r1[[4, 0], [6, 2]])
