@@ -413,6 +413,7 @@ def bench_llm(peaks, configs=(0,), shapes=None):
         gw = float(w.abs().max().float() / (6 * 448))
         A, SFA = nv.quantize(x, gx)
         B, SFB = nv.quantize(w, gw)
+        A2, SP2 = nv.quantize_two_pass(x, gx) if K % 256 == 0 else (None, None)
         del x, w
         sfa, sfb = nv.pack_scales(SFA, K), nv.pack_scales(SFB, K)
         wbytes = B.numel() + sfb.numel()
@@ -428,10 +429,12 @@ def bench_llm(peaks, configs=(0,), shapes=None):
         cell = {"bound": "tensor" if t_tensor >= t_hbm else "hbm",
                 "roofline_us": round(max(t_tensor, t_hbm), 2), "copies": copies}
         ws = torch.zeros(nv.gemm_streamk_workspace_bytes(), dtype=torch.uint8, device="cuda")
-        for cfg in list(configs) + ["streamk"]:
+        for cfg in list(configs) + ["streamk"] + (["two_pass"] if A2 is not None else []):
             def call(i, stream=None, cfg=cfg):
                 if cfg == "streamk":
                     nv.gemm_streamk(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, ws, out=D, stream=stream)
+                elif cfg == "two_pass":
+                    nv.gemm_two_pass(A2, SP2, Bs[i], sfbs[i], alpha, M, N, K, out=D, stream=stream)
                 else:
                     nv.gemm(A, sfa, Bs[i], sfbs[i], alpha, M, N, K, out=D, config=cfg, stream=stream)
             for i in range(2):
@@ -457,13 +460,21 @@ def bench_llm(peaks, configs=(0,), shapes=None):
                 us = e0.elapsed_time(e1) * 1e3 / copies
                 best = us if best is None else min(best, us)
             del g
-            key = cfg if cfg == "streamk" else ("auto" if cfg == 0 else f"config{cfg}")
-            cell[key] = {"us": round(best, 2), "tflops": round(flops / best / 1e6, 1),
-                         "roofline_frac": round(max(t_tensor, t_hbm) / best, 3)}
+            key = cfg if cfg in ("streamk", "two_pass") else ("auto" if cfg == 0 else f"config{cfg}")
+            if cfg == "two_pass":
+                # twice the MMA work; the activation operand is twice as large
+                f2 = 2 * flops
+                b2 = nbytes + M * K // 2 + M * K // 16
+                r2 = max(f2 / (peak_fp4 * 1e12) * 1e6, b2 / (peaks["hbm_gbs"] * 1e9) * 1e6)
+                cell[key] = {"us": round(best, 2), "tflops": round(f2 / best / 1e6, 1),
+                             "roofline_us": round(r2, 2), "roofline_frac": round(r2 / best, 3)}
+            else:
+                cell[key] = {"us": round(best, 2), "tflops": round(flops / best / 1e6, 1),
+                             "roofline_frac": round(max(t_tensor, t_hbm) / best, 3)}
         if 0 in configs:
             cell["auto_config"] = nv.gemm_config_name(nv.gemm_choose_config(M, N, K)).split(" ")[0]
         out[f"M{M}_N{N}_K{K}"] = cell
-        del A, B, SFA, SFB, sfa, sfb, D, Bs, sfbs, ws
+        del A, B, SFA, SFB, sfa, sfb, D, Bs, sfbs, ws, A2, SP2
     err = nv.device_error()
     if err != 0:
         raise RuntimeError(f"device error {err}")
@@ -524,7 +535,13 @@ def bench_producers(peaks):
     sfps = [torch.empty(nv.packed_scales_bytes(R, K), dtype=torch.uint8, device="cuda") for _ in range(n)]
     calls = [lambda st, i=i: nv.quantize_packed(xs[i], g, codes[i], sfps[i], stream=st) for i in range(n)]
     res["quantize_packed"] = graph_time(calls, qbytes)
-    del xs, codes, sfps
+    # two-pass quantise: same reads, twice the codes and scales (packed) written
+    tbytes = R * K * 2 + R * K + R * K // 8
+    c2s = [torch.empty((R, K), dtype=torch.uint8, device="cuda") for _ in range(n)]
+    s2s = [torch.empty(nv.packed_scales_bytes(R, 2 * K), dtype=torch.uint8, device="cuda") for _ in range(n)]
+    calls = [lambda st, i=i: nv.quantize_two_pass(xs[i], g, c2s[i], s2s[i], stream=st) for i in range(n)]
+    res["quantize_two_pass"] = graph_time(calls, tbytes)
+    del xs, codes, sfps, c2s, s2s
     # pack_scales: 1 B in, 1 B out per scale
     pbytes = 2 * R * K // 16
     n = max(2, int(np.ceil(4 * l2 / pbytes)))

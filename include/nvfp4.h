@@ -108,6 +108,33 @@ nvfp4_status nvfp4_quantize_packed(const void* x_bf16, int64_t rows, int64_t K, 
                                    uint8_t* codes, uint8_t* sf_packed, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_two_pass -- BF16 activations -> a two-pass (value + residual) NVFP4
+ * operand for nvfp4_gemm_two_pass.
+ *
+ * [P2] follow-ups: activations quantised in two NVFP4 passes, value and residual,
+ * both consumed by the block-scaled FP4 MMA.  The page gives no formula; this
+ * library reads it as
+ *   q1 = nvfp4_quantize(x, global_scale)
+ *   r  = x - (value(q1 code) * q1 scale) * global_scale     (IEEE float32 steps:
+ *        the product is exact, the multiply and the subtraction each round)
+ *   q2 = the same quantiser applied to r, with the same global_scale,
+ * so that x ~ (dq1 + dq2) * global_scale and one GEMM alpha serves both passes.
+ *
+ *   x_bf16, rows, global_scale   as nvfp4_quantize.
+ *   K           K >= 256 and K % 256 == 0 (else NVFP4_ERR_UNSUPPORTED_SHAPE).
+ *   codes2      [rows x K] bytes out (2K codes per row), 8-byte aligned: for each
+ *               256-element K-block j of x, bytes [256j, 256j + 128) hold q1's codes of
+ *               that block and bytes [256j + 128, 256j + 256) q2's codes of the same
+ *               elements (low nibble = even k, as everywhere).
+ *   sf2_packed  nvfp4_packed_scales_bytes(rows, 2 * K) bytes out, 16-byte aligned:
+ *               the packed layout of a [rows x 2K] operand whose scale column 32j + u
+ *               is q1's scale u of K-block j (u < 16) and 32j + 16 + u is q2's.
+ * Bytes equal the IEEE reading above on every input without NaN.
+ */
+nvfp4_status nvfp4_quantize_two_pass(const void* x_bf16, int64_t rows, int64_t K, float global_scale,
+                                     uint8_t* codes2, uint8_t* sf2_packed, nvfp4_stream_t stream);
+
+/*
  * Size in bytes of the packed scale-factor buffer of a [rows x K] operand:
  * ceil(rows/128)*128 * ceil(K/64)*4.  Returns 0 for rows < 1 or K < 16 or K % 16 != 0.
  */
@@ -222,6 +249,27 @@ size_t nvfp4_gemm_streamk_workspace_bytes(void);
 nvfp4_status nvfp4_gemm_streamk_noalloc(const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
                                         const uint8_t* SFB, float alpha, void* D_bf16, int64_t M, int64_t N,
                                         int64_t K, int reset_scratch, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm_two_pass -- D = bf16(alpha * sum_k (dq1[m,k] + dq2[m,k]) * (B*SFB)[n,k]),
+ * FP32 accumulation, for a two-pass activation from nvfp4_quantize_two_pass
+ * ([P2] follow-ups, value + residual on the block-scaled FP4 MMA).
+ *
+ * Both passes run on the same tcgen05 kernels as nvfp4_gemm, into one accumulator:
+ * the kernels walk the activation's 2K codes and use each 256-element K-block of
+ * the weight twice (once for the value block, once for the residual block), so
+ * the weight is read from memory once per output tile, as in nvfp4_gemm.
+ *
+ *   A2, SFA2   codes2 and sf2_packed of nvfp4_quantize_two_pass for [M x K].
+ *   B, SFB     the weight as for nvfp4_gemm: [N x K/2] codes, packed scales of [N x K].
+ *   alpha      finite FP32 (global scale of the activation x that of the weight).
+ *   D_bf16, M, N   as nvfp4_gemm.
+ *   K          the weight's K: K >= 256 and K % 256 == 0.
+ * Accuracy: |D - exact| <= 2^-8 |exact| + 1e-6 |alpha| sum_k (|dq1_k| + |dq2_k|) |b_k|.
+ * Deterministic.  Errors as nvfp4_gemm, plus NVFP4_ERR_UNSUPPORTED_SHAPE for K % 256.
+ */
+nvfp4_status nvfp4_gemm_two_pass(const uint8_t* A2, const uint8_t* SFA2, const uint8_t* B, const uint8_t* SFB,
+                                 float alpha, void* D_bf16, int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream);
 
 /* Name of a GEMM kernel configuration, or NULL past the last one (config >= 1). */
 const char* nvfp4_gemm_config_name(int config);

@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "l
 
 #: Every symbol include/nvfp4.h declares.
 ABI_SYMBOLS = (
-    "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_quantize_packed", "nvfp4_packed_scales_bytes",
+    "nvfp4_status_string", "nvfp4_version", "nvfp4_quantize", "nvfp4_quantize_packed",
+    "nvfp4_quantize_two_pass", "nvfp4_gemm_two_pass", "nvfp4_packed_scales_bytes",
     "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_streamk",
     "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_streamk_noalloc", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
@@ -58,6 +59,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_version": (c_i, []),
         "nvfp4_quantize": (c_i, [c_p, c_i64, c_i64, c_f, c_p, c_p, c_p]),
         "nvfp4_quantize_packed": (c_i, [c_p, c_i64, c_i64, c_f, c_p, c_p, c_p]),
+        "nvfp4_quantize_two_pass": (c_i, [c_p, c_i64, c_i64, c_f, c_p, c_p, c_p]),
+        "nvfp4_gemm_two_pass": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_packed_scales_bytes": (ctypes.c_size_t, [c_i64, c_i64]),
         "nvfp4_pack_scales": (c_i, [c_p, c_i64, c_i64, c_p, c_p]),
         "nvfp4_gemm": (c_i, [c_p, c_p, c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
@@ -164,6 +167,29 @@ def quantize_packed(x, global_scale: float, codes=None, sf_packed=None, stream=N
     return codes, sf_packed
 
 
+def quantize_two_pass(x, global_scale: float, codes2=None, sf2_packed=None, stream=None):
+    """bf16 [rows, K] -> (codes2 uint8 [rows, K] (value and residual K-blocks of 256
+    interleaved), packed scales uint8 [packed_scales_bytes(rows, 2K)])."""
+    import torch
+
+    _cuda(x, "x", torch.bfloat16)
+    rows, K = x.shape
+    n = packed_scales_bytes(rows, 2 * K)
+    if codes2 is None:
+        codes2 = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    if sf2_packed is None:
+        sf2_packed = torch.empty((n,), dtype=torch.uint8, device=x.device)
+    _cuda(codes2, "codes2", torch.uint8)
+    _cuda(sf2_packed, "sf2_packed", torch.uint8)
+    if codes2.numel() < rows * K:
+        raise ValueError(f"codes2 holds {codes2.numel()} bytes, needs {rows * K}")
+    if sf2_packed.numel() < n:
+        raise ValueError(f"sf2_packed holds {sf2_packed.numel()} bytes, needs {n}")
+    _check("nvfp4_quantize_two_pass", load_library().nvfp4_quantize_two_pass(
+        _ptr(x), rows, K, float(global_scale), _ptr(codes2), _ptr(sf2_packed), _stream(stream)))
+    return codes2, sf2_packed
+
+
 def pack_scales(sf, K: int | None = None, out=None, stream=None):
     """Row-major scales [rows, K/16] -> packed 128x4-atom buffer (uint8, flat)."""
     import torch
@@ -231,6 +257,22 @@ def gemm_streamk_noalloc(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, o
     _check("nvfp4_gemm_streamk_noalloc", load_library().nvfp4_gemm_streamk_noalloc(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
         1 if reset_scratch else 0, _stream(stream)))
+    return out
+
+
+def gemm_two_pass(A2, SFA2, B, SFB, alpha: float, M: int, N: int, K: int, out=None, stream=None):
+    """D = bf16(alpha (dq1 + dq2) w^T) for a two-pass activation from quantize_two_pass;
+    K is the weight's K (A2 holds 2K codes per row)."""
+    import torch
+
+    for t, nm in ((A2, "A2"), (SFA2, "SFA2"), (B, "B"), (SFB, "SFB")):
+        _cuda(t, nm, torch.uint8)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A2.device)
+    _cuda(out, "out", torch.bfloat16)
+    _check("nvfp4_gemm_two_pass", load_library().nvfp4_gemm_two_pass(
+        _ptr(A2), _ptr(SFA2), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
+        _stream(stream)))
     return out
 
 

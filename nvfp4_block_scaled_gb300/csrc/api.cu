@@ -194,6 +194,18 @@ nvfp4_status nvfp4_quantize_packed(const void* x_bf16, int64_t rows, int64_t K, 
   return launch_quantize(x_bf16, rows, K, global_scale, codes, sf_packed, true, as_stream(stream), dev);
 }
 
+nvfp4_status nvfp4_quantize_two_pass(const void* x_bf16, int64_t rows, int64_t K, float global_scale,
+                                     uint8_t* codes2, uint8_t* sf2_packed, nvfp4_stream_t stream) {
+  nvfp4_status st = quantize_checks(x_bf16, rows, K, global_scale, codes2, sf2_packed);
+  if (st != NVFP4_OK) return st;
+  if (K % 256 != 0 || 2 * K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(sf2_packed, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_quantize_two_pass(x_bf16, rows, K, global_scale, codes2, sf2_packed, as_stream(stream), dev);
+}
+
 size_t nvfp4_packed_scales_bytes(int64_t rows, int64_t K) {
   if (rows < 1 || K < 16 || K % 16 != 0 || rows > kMaxDim || K > kMaxDim) return 0;
   return static_cast<size_t>((rows + 127) / 128) * 128 * static_cast<size_t>((K + 63) / 64) * 4;
@@ -262,6 +274,17 @@ nvfp4_status nvfp4_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uint
   if (need == 0) return NVFP4_ERR_CUDA;
   if (workspace_bytes < need) return NVFP4_ERR_INVALID_ARG;
   return launch_gemm_streamk(A, SFA, B, SFB, alpha, D_bf16, M, N, K, workspace, as_stream(stream), dev);
+}
+
+nvfp4_status nvfp4_gemm_two_pass(const uint8_t* A2, const uint8_t* SFA2, const uint8_t* B, const uint8_t* SFB,
+                                 float alpha, void* D_bf16, int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream) {
+  nvfp4_status st = gemm_checks(A2, SFA2, B, SFB, alpha, D_bf16, M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (K % 256 != 0 || 2 * K > kMaxDim) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return launch_gemm_two_pass(A2, SFA2, B, SFB, alpha, D_bf16, M, N, K, as_stream(stream), dev);
 }
 
 const char* nvfp4_gemm_config_name(int config) { return gemm_config_name(config); }

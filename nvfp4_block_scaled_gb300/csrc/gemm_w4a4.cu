@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const uint8_t* __restrict__ SFA, const uint8_t* __restrict__ SFB,
                      __nv_bfloat16* __restrict__ D, float alpha, int M, int N, int K, int tiles_m,
-                     int tiles_n, int group_n) {
+                     int tiles_n, int group_n, int b_shift) {
   using C = Cfg<BN, STAGES, ACC_BUFS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -187,10 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bytes = C::kABytes + C::kBBytes + nk * kAtom * (1 + nbv);
           const uint32_t fb = bar_full + 8 * stage;
           mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sbase + C::kOffB + stage * C::kBBytes, &tmB, fb, kb * kBKBytes, nb * BN, pol);
+          tma_load_2d(sbase + C::kOffB + stage * C::kBBytes, &tmB, fb, (kb >> b_shift) * kBKBytes, nb * BN, pol);
           for (int b = 0; b < nbv; ++b)
             bulk_load(sbase + C::kOffSFB + stage * C::kSFBBytes + b * kKSteps * kAtom,
-                      SFB + (static_cast<size_t>(nb * C::kBands + b) * KG + kb * kKSteps) * kAtom,
+                      SFB + (static_cast<size_t>(nb * C::kBands + b) * (KG >> b_shift) + (kb >> b_shift) * kKSteps) *
+                                kAtom,
                       nk * kAtom, fb, pol);
           if (dfr.done) load_a(stage, kb, mb, nk); else dfr.add(stage, kb, mb, nk);
           ++issued;
@@ -326,7 +327,7 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(kSplitThreads, 1)
     gemm_nvf4_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const uint8_t* __restrict__ SFA, const uint8_t* __restrict__ SFB,
-                            __nv_bfloat16* __restrict__ D, float alpha, int M, int N, int K, int S) {
+                            __nv_bfloat16* __restrict__ D, float alpha, int M, int N, int K, int S, int b_shift) {
   using C = Cfg<BN, STAGES, 1>;
   // The receive slots (at most S x 128 rows x (ceil(BN/8 / S) x 32 + 16) bytes, largest
   // for S = 6 or 7) fit in the drained operand ring, below the per-unit table at its end.
@@ -398,11 +399,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         const int nk = min(kKSteps, KG - kb * kKSteps);
         const uint32_t fb = bar_full + 8 * stage;
         mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes + nk * kAtom * (1 + nbv));
-        tma_load_2d(sbase + C::kOffB + stage * C::kBBytes, &tmB, fb, kb * kBKBytes, nb * BN, pol);
+        tma_load_2d(sbase + C::kOffB + stage * C::kBBytes, &tmB, fb, (kb >> b_shift) * kBKBytes, nb * BN, pol);
         for (int b = 0; b < nbv; ++b)
           bulk_load(sbase + C::kOffSFB + stage * C::kSFBBytes + b * kKSteps * kAtom,
-                    SFB + (static_cast<size_t>(nb * C::kBands + b) * KG + kb * kKSteps) * kAtom, nk * kAtom, fb,
-                    pol);
+                    SFB + (static_cast<size_t>(nb * C::kBands + b) * (KG >> b_shift) + (kb >> b_shift) * kKSteps) *
+                              kAtom,
+                    nk * kAtom, fb, pol);
         if (dfr.done) load_a(stage, kb, mb, nk); else dfr.add(stage, kb, mb, nk);
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -705,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                           const __grid_constant__ CUtensorMap tmD, float alpha, int K, int tiles_m, int tiles_n,
-                          int group_n, float* __restrict__ ws, uint32_t* __restrict__ flags) {
+                          int group_n, float* __restrict__ ws, uint32_t* __restrict__ flags, int b_shift) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -788,8 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
           const uint32_t fb = full_leader + 8 * stage;
-          tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * kb);
-          tma_load_3d_pair(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, kb * kStepsP, nt * 2);
+          tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * (kb >> b_shift));
+          tma_load_3d_pair(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, (kb >> b_shift) * kStepsP, nt * 2);
           if (dfr.done) load_a(stage, kb, mt, 0); else dfr.add(stage, kb, mt, 0);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -1046,7 +1048,8 @@ inline void set_programmatic(cudaLaunchAttribute& a) {
 
 template <int BN, int STAGES, int ACC_BUFS>
 nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
-                 void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+                 void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev,
+                 int b_shift = 0) {
   using C = Cfg<BN, STAGES, ACC_BUFS>;
   auto kern = gemm_nvf4_kernel<BN, STAGES, ACC_BUFS>;
   static bool attr_set[64] = {};
@@ -1058,7 +1061,8 @@ nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const u
   CUtensorMap ta, tb;
   nvfp4_status st = encode_tmap_u8_2d(&ta, A, K / 2, M, K / 2, kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != NVFP4_OK) return st;
-  st = encode_tmap_u8_2d(&tb, B, K / 2, N, K / 2, kBKBytes, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  st = encode_tmap_u8_2d(&tb, B, (K >> b_shift) / 2, N, (K >> b_shift) / 2, kBKBytes, BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != NVFP4_OK) return st;
   const int tiles_m = static_cast<int>((M + kBM - 1) / kBM);
   const int tiles_n = static_cast<int>((N + BN - 1) / BN);
@@ -1076,7 +1080,7 @@ nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const u
   cfg.numAttrs = 1;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, SFA, SFB, static_cast<__nv_bfloat16*>(D), alpha,
                                       static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), tiles_m, tiles_n,
-                                      group_n));
+                                      group_n, b_shift));
 }
 
 // K split for a shape.  Clusters of S CTAs (one CTA per SM) must fit inside a GPC,
@@ -1100,7 +1104,8 @@ int splitk_factor(int64_t tiles, int64_t K, const int (&active)[9]) {
 
 template <int BN, int STAGES>
 nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
-                        void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+                        void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev,
+                        int b_shift = 0) {
   using C = Cfg<BN, STAGES, 1>;
   auto kern = gemm_nvf4_splitk_kernel<BN, STAGES>;
   static bool attr_set[64] = {};
@@ -1129,12 +1134,14 @@ nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
   }
   const int64_t tiles_m = (M + kBM - 1) / kBM;
   const int64_t tiles_n = (N + BN - 1) / BN;
-  if (tiles_m > 65535 || tiles_n > 65535) return run<BN, STAGES, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+  if (tiles_m > 65535 || tiles_n > 65535)
+    return run<BN, STAGES, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
   const int S = splitk_factor(tiles_m * tiles_n, K, active[d]);
   CUtensorMap ta, tb;
   nvfp4_status st = encode_tmap_u8_2d(&ta, A, K / 2, M, K / 2, kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != NVFP4_OK) return st;
-  st = encode_tmap_u8_2d(&tb, B, K / 2, N, K / 2, kBKBytes, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  st = encode_tmap_u8_2d(&tb, B, (K >> b_shift) / 2, N, (K >> b_shift) / 2, kBKBytes, BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != NVFP4_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, static_cast<unsigned>(tiles_n), static_cast<unsigned>(tiles_m));
@@ -1150,7 +1157,7 @@ nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, SFA, SFB, static_cast<__nv_bfloat16*>(D), alpha,
-                                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), S));
+                                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), S, b_shift));
 }
 
 // Pairs that can be co-resident (cudaOccupancyMaxActiveClusters for clusters of
@@ -1194,17 +1201,17 @@ size_t streamk_bytes(int pairs) { return streamk_flags_bytes(pairs) + static_cas
 // the data-parallel schedule.
 nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
                       void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev,
-                      bool streamk = false, void* ws = nullptr) {
+                      bool streamk = false, void* ws = nullptr, int b_shift = 0) {
   const int slots = pair_slots(dev);
   if (slots < 0) return NVFP4_ERR_CUDA;
   CUtensorMap ta, tb, tsfa, tsfb, td;
   // A and B as [K/256 chunks][rows][128 bytes]: one box = 128 rows x one stage's chunks.
   nvfp4_status st = encode_tmap_u8_3d_chunks(&ta, A, M, K, 128, pair::kBKP / 256);
-  if (st == NVFP4_OK) st = encode_tmap_u8_3d_chunks(&tb, B, N, K, 128, pair::kBKP / 256);
+  if (st == NVFP4_OK) st = encode_tmap_u8_3d_chunks(&tb, B, N, K >> b_shift, 128, pair::kBKP / 256);
   // Packed scales as [bands][K/64 atoms][128 x u32]: SFA box = one stage's atoms of one
   // band, SFB box = one stage's atoms of two bands.
   if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfa, SFA, M, K, pair::kStepsP, 1);
-  if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfb, SFB, N, K, pair::kStepsP, 2);
+  if (st == NVFP4_OK) st = encode_tmap_sf_3d(&tsfb, SFB, N, K >> b_shift, pair::kStepsP, 2);
   if (st == NVFP4_OK)
     st = encode_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, N, M, N * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != NVFP4_OK) return st;
@@ -1242,7 +1249,7 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   cfg.numAttrs = 2;
   auto kern = use_sk ? pair::gemm_nvf4_pair_kernel<true> : pair::gemm_nvf4_pair_kernel<false>;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, tsfa, tsfb, td, alpha, static_cast<int>(K), tiles_m,
-                                      tiles_n, group_n, part, flags));
+                                      tiles_n, group_n, part, flags, b_shift));
 }
 
 }  // namespace
@@ -1298,17 +1305,27 @@ nvfp4_status launch_gemm_streamk(const uint8_t* A, const uint8_t* SFA, const uin
 
 nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
                          const uint8_t* SFB, float alpha, void* D, int64_t M, int64_t N, int64_t K,
-                         cudaStream_t stream, const DeviceInfo& dev) {
+                         cudaStream_t stream, const DeviceInfo& dev, int b_shift) {
   switch (config) {
-    case 1: return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
-    case 2: return run<128, 4, 2>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+    case 1: return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
+    case 2: return run<128, 4, 2>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
     case 3:
-      if (K % 256 != 0) return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
-      return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
-    case 4: return run_splitk<256, 3>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
-    case 5: return run_splitk<128, 4>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev);
+      if (K % 256 != 0) return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
+      return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, false, nullptr, b_shift);
+    case 4: return run_splitk<256, 3>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
+    case 5: return run_splitk<128, 4>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
     default: return NVFP4_ERR_INVALID_ARG;
   }
+}
+
+nvfp4_status launch_gemm_two_pass(const uint8_t* A2, const uint8_t* SFA2, const uint8_t* B, const uint8_t* SFB,
+                                  float alpha, void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                                  const DeviceInfo& dev) {
+  // The activation operand holds 2K codes (value and residual K-blocks interleaved),
+  // so every kernel runs over 2K with the weight's K-block index halved: each weight
+  // stage is used by one value and one residual K-block, into one accumulator.
+  const int64_t K2 = 2 * K;
+  return launch_gemm(gemm_choose_config(M, N, K2, dev), A2, SFA2, B, SFB, alpha, D, M, N, K2, stream, dev, 1);
 }
 
 }  // namespace nvfp4

@@ -68,13 +68,24 @@ nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, ui
                              uint8_t* sf, bool packed, cudaStream_t stream, const DeviceInfo& dev);
 nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
+// Two-pass quantisation: codes [rows x K] bytes (2K codes, value and residual
+// K-blocks of 256 interleaved), scales packed for a [rows x 2K] operand; K % 256 == 0.
+nvfp4_status launch_quantize_two_pass(const void* x, int64_t rows, int64_t K, float g, uint8_t* codes,
+                                      uint8_t* sf_packed, cudaStream_t stream, const DeviceInfo& dev);
 
 int gemm_num_configs();
 const char* gemm_config_name(int config);
 int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+// b_shift = 1: B (and SFB) hold K >> 1 elements per row, and A's K-block kb meets
+// B's K-block kb >> 1 (the two-pass activation layout); 0 for a plain GEMM.
 nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,
                          const uint8_t* SFB, float alpha, void* D, int64_t M, int64_t N, int64_t K,
-                         cudaStream_t stream, const DeviceInfo& dev);
+                         cudaStream_t stream, const DeviceInfo& dev, int b_shift = 0);
+// Two-pass W4A4 GEMM: A2/SFA2 hold the value and residual codes of a [M x K]
+// activation interleaved per 256-element K-block (2K codes per row); B is [N x K].
+nvfp4_status launch_gemm_two_pass(const uint8_t* A2, const uint8_t* SFA2, const uint8_t* B, const uint8_t* SFB,
+                                  float alpha, void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                                  const DeviceInfo& dev);
 
 // Stream-K GEMM: workspace bytes for the current device, and the launch (falls back
 // to launch_gemm's automatic configuration for shapes the CTA-pair kernel does not take).

@@ -40,17 +40,28 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
   return r;
 }
 
-// Quantise one 16-element block: v0, v1 = its 32 bytes of bf16.  Returns the E4M3
-// scale byte and writes the 16 codes (little-endian nibbles) to *c0, *c1.
-__device__ __forceinline__ uint32_t quantize_block(uint4 v0, uint4 v1, float g, uint32_t* c0_out,
-                                                   uint32_t* c1_out) {
+// Exact value of an E2M1 code nibble: bit 3 sign, bits 2..1 exponent (bias 1), bit 0
+// mantissa; 0 and 0.5 for exponent 0.
+__device__ __forceinline__ float e2m1_to_float(uint32_t n) {
+  const uint32_t e = (n >> 1) & 3u, m = n & 1u;
+  const float mag = e == 0 ? 0.5f * static_cast<float>(m) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (n & 8u) ? -mag : mag;
+}
+
+// The 16 floats of one block of bf16: v0, v1 = its 32 bytes.
+__device__ __forceinline__ void unpack_bf16x16(uint4 v0, uint4 v1, float (&f)[16]) {
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  float f[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
+}
+
+// Quantise one 16-element block of floats.  Returns the E4M3 scale byte and writes
+// the 16 codes (little-endian nibbles) to *c0, *c1.
+__device__ __forceinline__ uint32_t quantize_floats(const float (&f)[16], float g, uint32_t* c0_out,
+                                                    uint32_t* c1_out) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -73,6 +84,27 @@ __device__ __forceinline__ uint32_t quantize_block(uint4 v0, uint4 v1, float g, 
   *c0_out = c0;
   *c1_out = c1;
   return sbyte;
+}
+
+// Quantise one 16-element block of bf16 (v0, v1 = its 32 bytes).
+__device__ __forceinline__ uint32_t quantize_block(uint4 v0, uint4 v1, float g, uint32_t* c0_out,
+                                                   uint32_t* c1_out) {
+  float f[16];
+  unpack_bf16x16(v0, v1, f);
+  return quantize_floats(f, g, c0_out, c1_out);
+}
+
+// Residual of a quantised block: r_i = f_i - (value(code_i) * scale) * g, the product
+// exact (at most 5 significant bits), the multiply by g and the subtraction each one
+// IEEE float32 operation (no contraction).
+__device__ __forceinline__ void residual_block(const float (&f)[16], uint32_t c0, uint32_t c1, uint32_t sbyte,
+                                               float g, float (&r)[16]) {
+  const float sc = e4m3_to_float(sbyte);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t nib = ((i < 8 ? c0 : c1) >> (4 * (i & 7))) & 0xFu;
+    r[i] = __fsub_rn(f[i], __fmul_rn(__fmul_rn(e2m1_to_float(nib), sc), g));
+  }
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t nblocks,
@@ -138,6 +170,74 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
     for (int i = threadIdx.x; i < na * 128; i += blockDim.x) {
       const int a = i >> 7, wd = i & 127;
       dst[i] = tile[(32 * (wd & 3) + (wd >> 2)) * kQPPitch + a];
+    }
+    __syncthreads();
+  }
+}
+
+// Two-pass (value + residual) quantisation into the interleaved operand: per 256-
+// element K-block j of a row, the value codes (128 bytes) then the residual codes
+// (128 bytes), so a row holds 2K codes; the scales in the packed layout of a
+// [rows x 2K] operand, where K-block j's value scales fill atoms 8j..8j+3 and its
+// residual scales atoms 8j+4..8j+7.  One thread block of 16 warps per (128-row band,
+// pair of K-blocks 2p, 2p+1): lane l of a warp takes source block 32p + l of a row
+// (K-block j = 2p + l/16, position u = l mod 16) through both passes.  Its value
+// codes land at byte 256j + 8u of the row, its residual codes at 256j + 128 + 8u
+// (four 128-byte runs per warp and row), and its two scales are assembled into atom
+// words by shuffles as in quantize_packed_kernel: value word 8(l/16) + u/4 and
+// residual word 8(l/16) + 4 + u/4 of the tile's row.  Rows past `rows`, and the
+// missing second K-block of an odd K/256, give zero scales and no codes.
+constexpr int kTPPitch = 16 + 1;  // atom words per tile row (two K-blocks), padded
+
+__global__ void __launch_bounds__(kQPThreads) quantize_two_pass_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                       int64_t C, int64_t kblocks,
+                                                                       int64_t pairs_per_band, int64_t num_tiles,
+                                                                       float g, uint2* __restrict__ codes,
+                                                                       uint32_t* __restrict__ sf_packed) {
+  __shared__ uint32_t tile[128 * kTPPitch];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, u = lane & 15;
+  const int64_t groups = 8 * kblocks;  // scale atoms per band of the [rows x 2K] operand
+  for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    const int64_t band = t / pairs_per_band;
+    const int64_t p = t - band * pairs_per_band;
+    const int64_t j = 2 * p + half;
+    const bool col_ok = j < kblocks;
+    const int nj = kblocks - 2 * p < 2 ? 1 : 2;
+#pragma unroll 1
+    for (int rr = 0; rr < 128 / (kQPThreads / 32); ++rr) {
+      const int row = warp + (kQPThreads / 32) * rr;
+      const int64_t r = band * 128 + row;
+      uint32_t s1 = 0, s2 = 0;
+      if (col_ok && r < rows) {
+        const int64_t b = r * C + 16 * j + u;
+        float f[16];
+        unpack_bf16x16(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), f);
+        uint32_t c0, c1, d0, d1;
+        s1 = quantize_floats(f, g, &c0, &c1);
+        float rf[16];
+        residual_block(f, c0, c1, s1, g, rf);
+        s2 = quantize_floats(rf, g, &d0, &d1);
+        uint2* crow = codes + r * 2 * C + 32 * j;
+        __stcs(crow + u, make_uint2(c0, c1));
+        __stcs(crow + 16 + u, make_uint2(d0, d1));
+      }
+      const uint32_t a1 = s1 | (__shfl_down_sync(0xffffffffu, s1, 1) << 8);
+      const uint32_t w1 = a1 | (__shfl_down_sync(0xffffffffu, a1, 2) << 16);
+      const uint32_t a2 = s2 | (__shfl_down_sync(0xffffffffu, s2, 1) << 8);
+      const uint32_t w2 = a2 | (__shfl_down_sync(0xffffffffu, a2, 2) << 16);
+      if ((u & 3) == 0) {
+        tile[row * kTPPitch + 8 * half + (u >> 2)] = w1;
+        tile[row * kTPPitch + 8 * half + 4 + (u >> 2)] = w2;
+      }
+    }
+    __syncthreads();
+    uint32_t* dst = sf_packed + (band * groups + 16 * p) * 128;
+    for (int i = threadIdx.x; i < nj * 8 * 128; i += blockDim.x) {
+      const int a = i >> 7, wd = i & 127;
+      dst[i] = tile[(32 * (wd & 3) + (wd >> 2)) * kTPPitch + a];
     }
     __syncthreads();
   }
@@ -250,6 +350,20 @@ nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, ui
   return from_cuda(cudaLaunchKernelEx(&cfg, quantize_packed_kernel, static_cast<const uint4*>(x), rows, C, groups,
                                       tiles_per_band, num_tiles, g, reinterpret_cast<uint2*>(codes),
                                       reinterpret_cast<uint32_t*>(sf)));
+}
+
+nvfp4_status launch_quantize_two_pass(const void* x, int64_t rows, int64_t K, float g, uint8_t* codes,
+                                      uint8_t* sf_packed, cudaStream_t stream, const DeviceInfo& dev) {
+  const int64_t C = K / 16;
+  const int64_t kblocks = K / 256;
+  const int64_t pairs_per_band = (kblocks + 1) / 2;
+  const int64_t num_tiles = ((rows + 127) / 128) * pairs_per_band;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = programmatic_config(grid_for(num_tiles * kQPThreads, kQPThreads, dev, 4), kQPThreads, stream);
+  set_programmatic(cfg, attr);
+  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_two_pass_kernel, static_cast<const uint4*>(x), rows, C, kblocks,
+                                      pairs_per_band, num_tiles, g, reinterpret_cast<uint2*>(codes),
+                                      reinterpret_cast<uint32_t*>(sf_packed)));
 }
 
 nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out, cudaStream_t stream,
