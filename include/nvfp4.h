@@ -196,8 +196,8 @@ nvfp4_status nvfp4_gemm_config(const uint8_t* A, const uint8_t* SFA, const uint8
  * partial (written to the workspace) in a fixed order, so repeated calls are
  * bit-identical (not bit-identical to nvfp4_gemm, whose summation order differs).
  * The split is taken only where a cost model in K-blocks per pair, charging the
- * fix-up as 8 K-blocks, predicts a gain over the data-parallel waves (measured:
- * 1024x5120x17408 58 us against 85 us, 1024x5120x5120 31 against 36); otherwise, and
+ * fix-up as 16 K-blocks, predicts a gain over the data-parallel waves (measured:
+ * 1024x5120x17408 58 us against 85 us, 1024x5120x5120 31 against 35); otherwise, and
  * for shapes the pair kernel does not take, the call runs as nvfp4_gemm.
  *
  *   A, SFA, B, SFB, alpha, D_bf16, M, N, K   as nvfp4_gemm.

@@ -956,28 +956,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
       }
-#pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
-        const int col0 = h * 128 + c32 * 32;
-        uint32_t v[32];
-        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
+      // Drain the accumulator in four 32-column chunks: chunk c + 1 is loaded from TMEM
+      // while chunk c is converted and staged, and the accumulator goes back to the
+      // MMA issuer as soon as the last chunk is in registers.
+      const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 128);
+      auto stage_chunk = [&](uint32_t (&v)[32], int c32) {
         if (part != nullptr) {
-          // fixed order: this pair's stages, then the head pair's partial; the next
-          // chunk's loads go out before this one is used
-          float4 hn[8];
+          // fixed order: this pair's stages, then the head pair's partial (chunk 0's
+          // partial was fetched while the MMAs ran)
+          float4 hq[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) hn[i] = c32 < 3 ? __ldcg(part + ((c32 + 1) * 8 + i) * 32) : hp[i];
-          tc_wait_ld();
+          for (int i = 0; i < 8; ++i) hq[i] = c32 == 0 ? hp[i] : __ldcg(part + (c32 * 8 + i) * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + hp[i].x);
-            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + hp[i].y);
-            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + hp[i].z);
-            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + hp[i].w);
-            hp[i] = hn[i];
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + hq[i].x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + hq[i].y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + hq[i].z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + hq[i].w);
           }
-        } else {
-          tc_wait_ld();
         }
         const uint32_t box = out_base + (2 * h + (c32 >> 1)) * kOutBox + r * 128;
 #pragma unroll
@@ -991,13 +987,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(p0), "r"(p1), "r"(p2), "r"(p3)
                        : "memory");
         }
-      }
+      };
+      uint32_t va[32], vb[32];
+      tc_ld_32x32b_x32(trow, va);
+      tc_wait_ld(va);
+      tc_ld_32x32b_x32(trow + 32, vb);
+      stage_chunk(va, 0);
+      tc_wait_ld(vb);
+      tc_ld_32x32b_x32(trow + 64, va);
+      stage_chunk(vb, 1);
+      tc_wait_ld(va);
+      tc_ld_32x32b_x32(trow + 96, vb);
+      stage_chunk(va, 2);
+      tc_wait_ld(vb);
       // Accumulator read out: hand it back to the MMA issuer.
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_leader);
+      stage_chunk(vb, 3);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_cluster(acce_leader);
         const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb)
@@ -1192,7 +1202,7 @@ int pair_slots(const DeviceInfo& dev) {
 // Stream-K workspace: one flag per (pair, rank), padded to 1 KB, then one 128 x 256
 // FP32 partial tile per (pair, rank).
 constexpr size_t kPartialBytes = 128 * 256 * 4;
-constexpr int64_t kStreamKFixupKB = 8;
+constexpr int64_t kStreamKFixupKB = 16;
 size_t streamk_flags_bytes(int pairs) { return ((static_cast<size_t>(pairs) * 2 * 4 + 1023) / 1024) * 1024; }
 size_t streamk_bytes(int pairs) { return streamk_flags_bytes(pairs) + static_cast<size_t>(pairs) * 2 * kPartialBytes; }
 
@@ -1221,8 +1231,11 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   int use_sk = (streamk && ws != nullptr && num_tiles > slots && num_tiles % slots != 0) ? 1 : 0;
   if (use_sk) {
     // Cost per pair in K-blocks: data-parallel waves against whole waves plus an even
-    // share of the rest plus the fix-up (one partial written, one read back; about
-    // four microseconds, eight K-blocks).  Ties stay data-parallel.
+    // share of the rest plus the fix-up.  The fix-up (one partial written, one read
+    // back, about four microseconds) and the stream-K instantiation's slower
+    // data-parallel waves are charged together as 16 K-blocks, the value at which the
+    // measured 4096^3, 8192^3 and 8192 x 5120 x 5120 cases stay data-parallel and the
+    // 1024-token layers with 80 tiles split.  Ties stay data-parallel.
     const int64_t KB = K / pair::kBKP;
     const int64_t waves = (num_tiles + slots - 1) / slots;
     const int64_t whole = num_tiles / slots - 1;
