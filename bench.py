@@ -87,9 +87,15 @@ def all_max(x, world):
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replicas_value(ms_max, steps, flops_per_step, world):
+    """Whole-job TFLOP/s of `world` replicas that each ran `steps` steps, timed by the
+    slowest rank (ms_max = that rank's summed step time)."""
+    return world * steps * flops_per_step / (ms_max / 1e3) / 1e12
 
 
 def load_peaks():
@@ -593,7 +599,7 @@ def run_ours(args):
     ms_rank = sum(times)
     ms_max = all_max(ms_rank, world)
     flops = 2.0 * S ** 3
-    value = world * args.steps * flops / (ms_max / 1e3) / 1e12
+    value = replicas_value(ms_max, args.steps, flops, world)
     avg_ms = statistics.mean(times)
     achieved = flops / (avg_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"] * FP4_OVER_BF16
