@@ -1062,12 +1062,11 @@ nvfp4_status run(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const u
                  int b_shift = 0) {
   using C = Cfg<BN, STAGES, ACC_BUFS>;
   auto kern = gemm_nvf4_kernel<BN, STAGES, ACC_BUFS>;
-  static bool attr_set[64] = {};
-  if (dev.device < 64 && !attr_set[dev.device]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    attr_set[dev.device] = true;
-  }
+  static PerDeviceOnce smem_attr;
+  if (!smem_attr.get(dev.device, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess;
+      }))
+    return NVFP4_ERR_CUDA;
   CUtensorMap ta, tb;
   nvfp4_status st = encode_tmap_u8_2d(&ta, A, K / 2, M, K / 2, kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != NVFP4_OK) return st;
@@ -1118,12 +1117,12 @@ nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
                         int b_shift = 0) {
   using C = Cfg<BN, STAGES, 1>;
   auto kern = gemm_nvf4_splitk_kernel<BN, STAGES>;
-  static bool attr_set[64] = {};
+  static PerDeviceOnce setup;
   static int active[64][9] = {};  // co-resident clusters of S CTAs, per device
   const int d = dev.device < 64 ? dev.device : 63;
-  if (!attr_set[d]) {
+  const int ok = setup.get(d, [&] {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
+      return 0;
     for (int s = 1; s <= 8; ++s) {
       cudaLaunchConfig_t qc = {};
       qc.gridDim = dim3(s, 1, 1);
@@ -1140,8 +1139,9 @@ nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
       if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess) n = 0;
       active[d][s] = n > 0 ? n : dev.num_sms / s;
     }
-    attr_set[d] = true;
-  }
+    return 1;
+  });
+  if (!ok) return NVFP4_ERR_CUDA;
   const int64_t tiles_m = (M + kBM - 1) / kBM;
   const int64_t tiles_n = (N + BN - 1) / BN;
   if (tiles_m > 65535 || tiles_n > 65535)
@@ -1173,9 +1173,8 @@ nvfp4_status run_splitk(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, 
 // Pairs that can be co-resident (cudaOccupancyMaxActiveClusters for clusters of
 // two), queried once per device; also sets the kernel's shared-memory limit.
 int pair_slots(const DeviceInfo& dev) {
-  static int max_clusters[64] = {};
-  const int d = dev.device < 64 ? dev.device : 63;
-  if (max_clusters[d] == 0) {
+  static PerDeviceOnce slots;
+  return slots.get(dev.device, [&] {
     auto kern = pair::gemm_nvf4_pair_kernel<false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(pair::gemm_nvf4_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1194,9 +1193,8 @@ int pair_slots(const DeviceInfo& dev) {
     qc.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess || n < 1) n = dev.num_sms / 2;
-    max_clusters[d] = n;
-  }
-  return max_clusters[d];
+    return n;
+  });
 }
 
 // Stream-K workspace: one flag per (pair, rank), padded to 1 KB, then one 128 x 256

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -22,6 +23,21 @@ struct DeviceInfo {
 
 // Cached properties of the current device (queried once per device).
 nvfp4_status current_device(DeviceInfo* out);
+
+// One-time setup per device (kernel attributes, occupancy queries) that host threads
+// may reach concurrently: the first caller for a device runs `f`, callers arriving
+// meanwhile wait for it, and every later call returns the same result.  Each call
+// site owns its own instance (a function-local static).
+struct PerDeviceOnce {
+  std::once_flag flag[64];
+  int result[64] = {};
+  template <typename F>
+  int get(int device, F&& f) {
+    const int d = device >= 0 && device < 64 ? device : 63;
+    std::call_once(flag[d], [&] { result[d] = f(); });
+    return result[d];
+  }
+};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

@@ -397,13 +397,11 @@ nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float
   if (static_cast<size_t>(smem) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_DEVICE;
   // The dynamic shared-memory limit is raised once per device (no per-call attribute
   // changes, so calls can be captured in CUDA graphs).
-  static bool attr_set[64] = {};
-  const int d = dev.device < 64 ? dev.device : 63;
-  if (!attr_set[d]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    attr_set[d] = true;
-  }
+  static PerDeviceOnce smem_attr;
+  if (!smem_attr.get(dev.device, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+      }))
+    return NVFP4_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, N / 128, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
@@ -785,13 +783,13 @@ void choose_tc(int groups, int KC, int M, const int (&active)[9], int* S_out, in
 nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, const float* alpha_col, __nv_bfloat16* y,
                        int M, int N, int K, cudaStream_t stream, const DeviceInfo& dev) {
   auto kern = tcw::w4a16_tc_kernel;
-  static bool attr_set[64] = {};
+  static PerDeviceOnce setup;
   static int active[64][9] = {};  // co-resident clusters of S CTAs (one CTA per SM), per device
   const int d = dev.device < 64 ? dev.device : 63;
-  if (!attr_set[d]) {
+  const int ok = setup.get(d, [&] {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(dev.max_smem_optin)) != cudaSuccess)
-      return NVFP4_ERR_CUDA;
+      return 0;
     for (int s = 1; s <= 8; ++s) {
       cudaLaunchConfig_t qc = {};
       qc.gridDim = dim3(s, 1, 1);
@@ -808,8 +806,9 @@ nvfp4_status launch_tc(const CUtensorMap& tmW, const void* x, float alpha128, co
       if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess) n = 0;
       active[d][s] = n > 0 ? n : dev.num_sms / s;
     }
-    attr_set[d] = true;
-  }
+    return 1;
+  });
+  if (!ok) return NVFP4_ERR_CUDA;
   int S, nt, mt;
   choose_tc(N / 128, K / 64, M, active[d], &S, &nt, &mt);
   const tcw::Layout L = tcw::layout(nt);
