@@ -7,10 +7,14 @@ CUDA stream to the C ABI, and raise ``NVFP4Error`` on a non-OK status.  There is
 no CPU fallback: if the shared library has not been built, the first call raises.
 
 Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
-  quantize, quantize_packed, packed_scales_bytes, pack_scales, gemm, gemm_streamk,
-  gemm_streamk_workspace_bytes, gemm_config_name,
-  gemm_choose_config, w4a16_prepared_bytes, w4a16_prepare, w4a16_linear,
-  w4a16_linear_colscale, device_error.
+  quantize, quantize_packed, quantize_two_pass, packed_scales_bytes, pack_scales,
+  gemm, gemm_streamk, gemm_streamk_workspace_bytes, gemm_streamk_noalloc,
+  gemm_two_pass, gemm_config_name, gemm_choose_config, w4a16_prepared_bytes,
+  w4a16_prepare, w4a16_linear, w4a16_linear_colscale, device_error.
+
+Every entry point checks that each tensor it is given holds at least the bytes the
+call reads or writes (the C ABI takes raw pointers and cannot), and raises
+``ValueError`` before anything is launched otherwise.
 """
 
 from __future__ import annotations
@@ -116,6 +120,27 @@ def _cuda(t, name, dtype=None):
     return t
 
 
+def _need(t, name, nbytes):
+    """Raise unless tensor t holds at least nbytes bytes.  The C ABI takes raw pointers
+    and cannot see buffer sizes, so this is where a short buffer is caught before a
+    kernel reads or writes past it.  Skipped when the size is not positive (invalid
+    shapes are reported by the library's own argument checks)."""
+    have = t.numel() * t.element_size()
+    if nbytes > 0 and have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes, needs {nbytes}")
+
+
+def _gemm_buffers(A, SFA, B, SFB, out, M, N, K, a_k):
+    """Size checks shared by the GEMM entry points; a_k is the activation's K in codes
+    (K, or 2K for the two-pass operand)."""
+    M, N, K, a_k = int(M), int(N), int(K), int(a_k)
+    _need(A, "A", M * a_k // 2)
+    _need(SFA, "SFA", packed_scales_bytes(M, a_k) if M > 0 and a_k > 0 else 0)
+    _need(B, "B", N * K // 2)
+    _need(SFB, "SFB", packed_scales_bytes(N, K) if N > 0 and K > 0 else 0)
+    _need(out, "out", 2 * M * N)
+
+
 # ---------------------------------------------------------------- entry points
 
 def version() -> int:
@@ -142,6 +167,8 @@ def quantize(x, global_scale: float, codes=None, sf=None, stream=None):
         sf = torch.empty((rows, K // 16), dtype=torch.uint8, device=x.device)
     _cuda(codes, "codes", torch.uint8)
     _cuda(sf, "sf", torch.uint8)
+    _need(codes, "codes", rows * K // 2)
+    _need(sf, "sf", rows * (K // 16))
     _check("nvfp4_quantize", load_library().nvfp4_quantize(
         _ptr(x), rows, K, float(global_scale), _ptr(codes), _ptr(sf), _stream(stream)))
     return codes, sf
@@ -162,6 +189,7 @@ def quantize_packed(x, global_scale: float, codes=None, sf_packed=None, stream=N
     _cuda(sf_packed, "sf_packed", torch.uint8)
     if sf_packed.numel() < n:
         raise ValueError(f"sf_packed holds {sf_packed.numel()} bytes, needs {n}")
+    _need(codes, "codes", rows * K // 2)
     _check("nvfp4_quantize_packed", load_library().nvfp4_quantize_packed(
         _ptr(x), rows, K, float(global_scale), _ptr(codes), _ptr(sf_packed), _stream(stream)))
     return codes, sf_packed
@@ -216,6 +244,7 @@ def gemm(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, out=None, config:
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _cuda(out, "out", torch.bfloat16)
+    _gemm_buffers(A, SFA, B, SFB, out, M, N, K, K)
     lib = load_library()
     _check("nvfp4_gemm", lib.nvfp4_gemm_config(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
@@ -237,6 +266,7 @@ def gemm_streamk(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, workspace
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _cuda(out, "out", torch.bfloat16)
+    _gemm_buffers(A, SFA, B, SFB, out, M, N, K, K)
     _check("nvfp4_gemm_streamk", load_library().nvfp4_gemm_streamk(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
         _ptr(workspace), int(workspace.numel()), _stream(stream)))
@@ -254,6 +284,7 @@ def gemm_streamk_noalloc(A, SFA, B, SFB, alpha: float, M: int, N: int, K: int, o
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _cuda(out, "out", torch.bfloat16)
+    _gemm_buffers(A, SFA, B, SFB, out, M, N, K, K)
     _check("nvfp4_gemm_streamk_noalloc", load_library().nvfp4_gemm_streamk_noalloc(
         _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
         1 if reset_scratch else 0, _stream(stream)))
@@ -270,6 +301,7 @@ def gemm_two_pass(A2, SFA2, B, SFB, alpha: float, M: int, N: int, K: int, out=No
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A2.device)
     _cuda(out, "out", torch.bfloat16)
+    _gemm_buffers(A2, SFA2, B, SFB, out, M, N, K, 2 * int(K))
     _check("nvfp4_gemm_two_pass", load_library().nvfp4_gemm_two_pass(
         _ptr(A2), _ptr(SFA2), _ptr(B), _ptr(SFB), float(alpha), _ptr(out), int(M), int(N), int(K),
         _stream(stream)))
@@ -308,6 +340,8 @@ def w4a16_prepare(W, SW, out=None, stream=None):
     if out is None:
         out = torch.empty((max(n, 1),), dtype=torch.uint8, device=W.device)
     _cuda(out, "out", torch.uint8)
+    _need(SW, "SW", N * (K // 16))
+    _need(out, "out", n)
     _check("nvfp4_w4a16_prepare", load_library().nvfp4_w4a16_prepare(
         _ptr(W), _ptr(SW), N, K, _ptr(out), _stream(stream)))
     return out
@@ -323,6 +357,8 @@ def w4a16_linear(x, Wprep, alpha: float, N: int, out=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _cuda(out, "out", torch.bfloat16)
+    _need(Wprep, "Wprep", w4a16_prepared_bytes(int(N), K))
+    _need(out, "out", 2 * M * int(N))
     _check("nvfp4_w4a16_linear", load_library().nvfp4_w4a16_linear(
         _ptr(x), _ptr(Wprep), float(alpha), _ptr(out), M, int(N), K, _stream(stream)))
     return out
@@ -341,6 +377,8 @@ def w4a16_linear_colscale(x, Wprep, alpha_col, N: int, out=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _cuda(out, "out", torch.bfloat16)
+    _need(Wprep, "Wprep", w4a16_prepared_bytes(int(N), K))
+    _need(out, "out", 2 * M * int(N))
     _check("nvfp4_w4a16_linear_colscale", load_library().nvfp4_w4a16_linear_colscale(
         _ptr(x), _ptr(Wprep), _ptr(alpha_col), _ptr(out), M, int(N), K, _stream(stream)))
     return out
