@@ -58,6 +58,33 @@ __device__ __forceinline__ void unpack_bf16x16(uint4 v0, uint4 v1, float (&f)[16
   }
 }
 
+// E2M1 codes of the IEEE quotients fl(f[o+i] / denom), i = 0..7, computed without a
+// division per element.  r = 1/denom rounded once (IEEE), so q = fl(f * r) is within
+// a relative 2^-23 of f / denom and fl(f / denom) within 2^-24 of it: the correctly
+// rounded quotient lies strictly between fl(q * (1 - 2^-20)) and fl(q * (1 + 2^-20)).
+// The E2M1 conversion is monotonic, so when both ends of that bracket give the same
+// eight codes those are the codes of the quotients.  Otherwise (some element within a
+// few ulp of a rounding midpoint) the word is recomputed from the IEEE divisions.
+// Quotients too small to be normal floats lie far below the first midpoint (0.25) and
+// give code 0 at both ends, as they do exactly.
+__device__ __forceinline__ uint32_t codes_word(const float (&f)[16], int o, float r, float denom) {
+  constexpr float kLo = 1.0f - 0x1p-20f, kHi = 1.0f + 0x1p-20f;
+  float lo[8], hi[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float q = __fmul_rn(f[o + i], r);
+    lo[i] = __fmul_rn(q, kLo);
+    hi[i] = __fmul_rn(q, kHi);
+  }
+  const uint32_t a = e2m1x8(lo[0], lo[1], lo[2], lo[3], lo[4], lo[5], lo[6], lo[7]);
+  const uint32_t b = e2m1x8(hi[0], hi[1], hi[2], hi[3], hi[4], hi[5], hi[6], hi[7]);
+  if (a == b) return a;
+  float e[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e[i] = __fdiv_rn(f[o + i], denom);
+  return e2m1x8(e[0], e[1], e[2], e[3], e[4], e[5], e[6], e[7]);
+}
+
 // Quantise one 16-element block of floats.  Returns the E4M3 scale byte and writes
 // the 16 codes (little-endian nibbles) to *c0, *c1.
 __device__ __forceinline__ uint32_t quantize_floats(const float (&f)[16], float g, uint32_t* c0_out,
@@ -70,11 +97,17 @@ __device__ __forceinline__ uint32_t quantize_floats(const float (&f)[16], float 
   uint32_t c0 = 0, c1 = 0;
   if (sbyte != 0) {
     const float denom = __fmul_rn(e4m3_to_float(sbyte), g);
-    float q[16];
+    const float r = __frcp_rn(denom);
+    if (r <= 3.0e38f) {  // a finite reciprocal: products and a bracket (codes_word)
+      c0 = codes_word(f, 0, r, denom);
+      c1 = codes_word(f, 8, r, denom);
+    } else {             // denom so small that 1/denom overflows: divide
+      float q[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(f[i], denom);
-    c0 = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-    c1 = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+      for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(f[i], denom);
+      c0 = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+      c1 = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+    }
     // A code whose magnitude rounded to zero is written as +0 (clear its sign bit).
     const uint32_t nz0 = ((c0 & 0x77777777u) + 0x77777777u) & 0x88888888u;
     const uint32_t nz1 = ((c1 & 0x77777777u) + 0x77777777u) & 0x88888888u;

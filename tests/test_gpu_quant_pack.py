@@ -111,3 +111,25 @@ def test_quantize_packed_then_gemm():
     ref, abs_sum = O.gemm(Ah, SFAh, Bh, SFBh, alpha)
     from gpu_util import assert_within, host_f64
     assert_within(host_f64(D), ref, abs_sum, alpha, "quantize_packed -> gemm")
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_quantize_tiny_global_scale_byte_exact(packed):
+    # g = 1e-37 and values ~1e-39 (bfloat16 subnormals): the block scales are E4M3
+    # subnormals, scale * g is a float32 subnormal whose reciprocal overflows, and the
+    # quantiser divides element by element.  The codes are mostly non-zero.
+    R, K = 64, 512
+    x = O.f32_to_bf16_rne((np.random.default_rng(4).standard_normal((R, K)) * 1e-39).astype(np.float32))
+    g = 1e-37
+    wc, ws = O.quantize(x, g)
+    denom = (O.e4m3_table()[ws].astype(np.float32) * np.float32(g)).astype(np.float32)
+    with np.errstate(over="ignore", divide="ignore"):
+        assert np.isinf(np.float32(1) / denom[ws > 0]).all()  # the path under test is reached
+    assert (O.unpack_codes(wc) != 0).mean() > 0.5
+    if packed:
+        codes, sfp = nv.quantize_packed(dev_bf16(x), g)
+        assert np.array_equal(sfp.cpu().numpy(), O.pack_scales(ws))
+    else:
+        codes, sf = nv.quantize(dev_bf16(x), g)
+        assert np.array_equal(sf.cpu().numpy(), ws)
+    assert np.array_equal(codes.cpu().numpy(), wc)
