@@ -154,19 +154,23 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
   }
 }
 
-// Fused quantize + pack.  One thread block of 16 warps per (128-row band, 8 atoms
-// = 32 scale columns): warp w quantises rows w, w+16, ..., w+112 of the band, lane
-// l the block in scale column 32*tile + l of each (a warp reads 1 KB and writes 256
-// bytes of codes contiguously).  Two shuffles assemble each 4-scale word of an
-// atom into a shared-memory tile, which is then written atom by atom, 512
-// contiguous bytes each (word w of an atom holds row 32*(w%4) + w/4): scattered
-// single-byte scale stores in the layout cost more than the separate packing pass.
-// Rows past `rows` and scale columns past C give zero scale bytes and no codes.
-// (16 warps per block: the quantiser is bound by chains of IEEE divisions, so it
-// wants the SM's full 64 warps.)
-constexpr int kQPAtoms = 8;
-constexpr int kQPPitch = kQPAtoms + 1;  // words per tile row (odd: spreads the banks)
+// Fused quantize + pack.  One thread block of 16 warps per (128-row band, 2 atoms
+// = 8 scale columns): lane l of a warp takes scale column 8*tile + l%8 of row
+// 4*(16*rr + w) + l/8 (rr = 0, 1), so a warp quantises four rows per step, reading
+// 256 contiguous bytes of each.  Two shuffles assemble each 4-scale word of an atom
+// into a shared-memory tile, which is then written atom by atom, 512 contiguous
+// bytes each (word w of an atom holds row 32*(w%4) + w/4): scattered single-byte
+// scale stores in the layout cost more than the separate packing pass.  Small tiles
+// keep the last wave short: 8192 x 5120 is 2560 tiles for 304 resident blocks (with
+// 8-atom tiles, 640 tiles took three rounds where 2.1 would do).  Rows past `rows`
+// and scale columns past C give zero scale bytes and no codes.  (16 warps per block:
+// the quantiser is bound by its arithmetic, so it wants the SM's full 64 warps.)
+constexpr int kQPAtoms = 2;
+constexpr int kQPCols = 4 * kQPAtoms;        // scale columns per tile = lanes per row
+constexpr int kQPRowsPerWarp = 32 / kQPCols; // rows per warp and step
+constexpr int kQPPitch = kQPAtoms + 1;       // words per tile row (odd: spreads the banks)
 constexpr int kQPThreads = 512;
+static_assert(32 % kQPCols == 0, "a warp covers whole rows of a tile");
 
 __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4* __restrict__ x, int64_t rows,
                                                                      int64_t C, int64_t groups, int64_t tiles_per_band,
@@ -177,15 +181,17 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = lane % kQPCols, rsub = lane / kQPCols;
+  constexpr int kWarps = kQPThreads / 32;
   for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
     const int64_t band = t / tiles_per_band;
     const int64_t a0 = (t - band * tiles_per_band) * kQPAtoms;
     const int na = static_cast<int>(groups - a0 < kQPAtoms ? groups - a0 : kQPAtoms);
-    const int64_t c = 4 * a0 + lane;
+    const int64_t c = 4 * a0 + col;
     const bool col_ok = c < C;
 #pragma unroll
-    for (int rr = 0; rr < 128 / (kQPThreads / 32); ++rr) {
-      const int row = warp + (kQPThreads / 32) * rr;
+    for (int rr = 0; rr < 128 / (kWarps * kQPRowsPerWarp); ++rr) {
+      const int row = (rr * kWarps + warp) * kQPRowsPerWarp + rsub;
       const int64_t r = band * 128 + row;
       uint32_t sbyte = 0;
       if (col_ok && r < rows) {
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
       }
       const uint32_t w1 = sbyte | (__shfl_down_sync(0xffffffffu, sbyte, 1) << 8);
       const uint32_t w2 = w1 | (__shfl_down_sync(0xffffffffu, w1, 2) << 16);
-      if ((lane & 3) == 0) tile[row * kQPPitch + (lane >> 2)] = w2;
+      if ((col & 3) == 0) tile[row * kQPPitch + (col >> 2)] = w2;
     }
     __syncthreads();
     uint32_t* dst = sf_packed + (band * groups + a0) * 128;
@@ -213,38 +219,35 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
 // (128 bytes), so a row holds 2K codes; the scales in the packed layout of a
 // [rows x 2K] operand, where K-block j's value scales fill atoms 8j..8j+3 and its
 // residual scales atoms 8j+4..8j+7.  One thread block of 16 warps per (128-row band,
-// pair of K-blocks 2p, 2p+1): lane l of a warp takes source block 32p + l of a row
-// (K-block j = 2p + l/16, position u = l mod 16) through both passes.  Its value
-// codes land at byte 256j + 8u of the row, its residual codes at 256j + 128 + 8u
-// (four 128-byte runs per warp and row), and its two scales are assembled into atom
-// words by shuffles as in quantize_packed_kernel: value word 8(l/16) + u/4 and
-// residual word 8(l/16) + 4 + u/4 of the tile's row.  Rows past `rows`, and the
-// missing second K-block of an odd K/256, give zero scales and no codes.
-constexpr int kTPPitch = 16 + 1;  // atom words per tile row (two K-blocks), padded
+// K-block j): lane l of a warp takes source block 16j + u (u = l mod 16) of row
+// 2*(16*rr + w) + l/16 (rr = 0..3) through both passes.  Its value codes land at
+// byte 256j + 8u of the row and its residual codes at 256j + 128 + 8u (two 128-byte
+// runs per row and pass), and its two scales are assembled into atom words by
+// shuffles as in quantize_packed_kernel: value word u/4 and residual word 4 + u/4
+// of the tile's row.  One K-block per tile keeps the last wave short (8192 x 5120 is
+// 1280 tiles for 304 resident blocks).  Rows past `rows` give zero scales and no codes.
+constexpr int kTPPitch = 8 + 1;  // atom words per tile row (one K-block), padded
 
 __global__ void __launch_bounds__(kQPThreads) quantize_two_pass_kernel(const uint4* __restrict__ x, int64_t rows,
-                                                                       int64_t C, int64_t kblocks,
-                                                                       int64_t pairs_per_band, int64_t num_tiles,
+                                                                       int64_t C, int64_t kblocks, int64_t num_tiles,
                                                                        float g, uint2* __restrict__ codes,
                                                                        uint32_t* __restrict__ sf_packed) {
   __shared__ uint32_t tile[128 * kTPPitch];
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, u = lane & 15;
+  const int u = lane & 15, rsub = lane >> 4;
+  constexpr int kWarps = kQPThreads / 32;
   const int64_t groups = 8 * kblocks;  // scale atoms per band of the [rows x 2K] operand
   for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const int64_t band = t / pairs_per_band;
-    const int64_t p = t - band * pairs_per_band;
-    const int64_t j = 2 * p + half;
-    const bool col_ok = j < kblocks;
-    const int nj = kblocks - 2 * p < 2 ? 1 : 2;
+    const int64_t band = t / kblocks;
+    const int64_t j = t - band * kblocks;
 #pragma unroll 1
-    for (int rr = 0; rr < 128 / (kQPThreads / 32); ++rr) {
-      const int row = warp + (kQPThreads / 32) * rr;
+    for (int rr = 0; rr < 128 / (2 * kWarps); ++rr) {
+      const int row = (rr * kWarps + warp) * 2 + rsub;
       const int64_t r = band * 128 + row;
       uint32_t s1 = 0, s2 = 0;
-      if (col_ok && r < rows) {
+      if (r < rows) {
         const int64_t b = r * C + 16 * j + u;
         float f[16];
         unpack_bf16x16(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), f);
@@ -262,13 +265,13 @@ __global__ void __launch_bounds__(kQPThreads) quantize_two_pass_kernel(const uin
       const uint32_t a2 = s2 | (__shfl_down_sync(0xffffffffu, s2, 1) << 8);
       const uint32_t w2 = a2 | (__shfl_down_sync(0xffffffffu, a2, 2) << 16);
       if ((u & 3) == 0) {
-        tile[row * kTPPitch + 8 * half + (u >> 2)] = w1;
-        tile[row * kTPPitch + 8 * half + 4 + (u >> 2)] = w2;
+        tile[row * kTPPitch + (u >> 2)] = w1;
+        tile[row * kTPPitch + 4 + (u >> 2)] = w2;
       }
     }
     __syncthreads();
-    uint32_t* dst = sf_packed + (band * groups + 16 * p) * 128;
-    for (int i = threadIdx.x; i < nj * 8 * 128; i += blockDim.x) {
+    uint32_t* dst = sf_packed + (band * groups + 8 * j) * 128;
+    for (int i = threadIdx.x; i < 8 * 128; i += blockDim.x) {
       const int a = i >> 7, wd = i & 127;
       dst[i] = tile[(32 * (wd & 3) + (wd >> 2)) * kTPPitch + a];
     }
@@ -389,13 +392,12 @@ nvfp4_status launch_quantize_two_pass(const void* x, int64_t rows, int64_t K, fl
                                       uint8_t* sf_packed, cudaStream_t stream, const DeviceInfo& dev) {
   const int64_t C = K / 16;
   const int64_t kblocks = K / 256;
-  const int64_t pairs_per_band = (kblocks + 1) / 2;
-  const int64_t num_tiles = ((rows + 127) / 128) * pairs_per_band;
+  const int64_t num_tiles = ((rows + 127) / 128) * kblocks;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = programmatic_config(grid_for(num_tiles * kQPThreads, kQPThreads, dev, 4), kQPThreads, stream);
   set_programmatic(cfg, attr);
   return from_cuda(cudaLaunchKernelEx(&cfg, quantize_two_pass_kernel, static_cast<const uint4*>(x), rows, C, kblocks,
-                                      pairs_per_band, num_tiles, g, reinterpret_cast<uint2*>(codes),
+                                      num_tiles, g, reinterpret_cast<uint2*>(codes),
                                       reinterpret_cast<uint32_t*>(sf_packed)));
 }
 
