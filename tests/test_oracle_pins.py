@@ -500,3 +500,156 @@ def test_gemm_two_pass_is_a_plain_gemm_over_the_interleaved_operand():
     assert np.array_equal(r1, r2) and np.array_equal(a1, a2)
     r3, _ = O.gemm_two_pass_at(c1, s1, c2, s2, B, SFB, 1.25, [4, 0], [6, 2])
     assert np.array_equal(r3, r1[[4, 0], [6, 2]])
+
+
+# ---------------------------------------------------------------- quantiser, step by step in exact arithmetic
+
+def _rn_f32(q):
+    """Round a Fraction to the nearest float32 value (ties to even), as a Fraction:
+    spacing 2^(e-23) in the binade [2^e, 2^(e+1)), 2^-149 below 2^-126."""
+    if q == 0:
+        return Fraction(0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    spacing = Fraction(2) ** (max(e, -126) - 23)
+    n = a / spacing
+    k = n.numerator // n.denominator
+    rem = n - k
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and k % 2 == 1):
+        k += 1
+    return sign * k * spacing
+
+
+def _nearest_even(v, values):
+    """Index of the nearest of the non-negative `values` to |v| (ties to the even index),
+    saturating at the largest."""
+    a = abs(v)
+    if a >= values[-1]:
+        return len(values) - 1
+    best = min(range(len(values)), key=lambda i: (abs(values[i] - a), i % 2))
+    return best
+
+
+def _e4m3_values():
+    return [Fraction(float(v)) for v in torch.arange(0x7F, dtype=torch.int32).to(torch.uint8)
+            .view(torch.float8_e4m3fn).double().numpy()]            # bytes 0x00..0x7E, ascending
+
+
+def _assert_quantize_matches_exact_steps(x, g, f32=False):
+    # Q2/Q3 applied with exact rationals and an explicit float32 rounding after each
+    # IEEE operation, the scale and the codes chosen by brute force over the formats'
+    # values: an implementation of the same reading that shares nothing with the
+    # oracle's numpy float32 arithmetic.
+    e4 = _e4m3_values()
+    e2 = [Fraction(m) for m in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    codes, sf = O.quantize_f32(x, g) if f32 else O.quantize(x, g)
+    cu = O.unpack_codes(codes)
+    gf = Fraction(float(np.float32(g)))
+    for b in range(x.shape[0]):
+        xs = [Fraction(float(v)) for v in (x[b].astype(np.float64) if f32 else O.bf16_bits_to_f64(x[b]))]
+        amax = max(abs(v) for v in xs)
+        s = _rn_f32(_rn_f32(amax / 6) / gf)
+        sbyte = _nearest_even(s, e4)
+        assert sf[b, 0] == sbyte, (b, g)
+        for k in range(16):
+            if sbyte == 0:
+                want = 0
+            else:
+                denom = _rn_f32(e4[sbyte] * gf)
+                v = _rn_f32(xs[k] / denom)
+                mag = _nearest_even(v, e2)
+                want = 0 if mag == 0 else mag | (8 if v < 0 else 0)
+            assert cu[b, k] == want, (b, k, g)
+
+
+def test_quantize_equals_exact_rational_steps():
+    rng = np.random.default_rng(12)
+    blocks = [G.bf16_normal(1, 16, s, "x")[0] for s in range(40)]
+    blocks += [O.f32_to_bf16_rne((rng.standard_normal(16) * 10.0 ** rng.uniform(-8, 4)).astype(np.float32))
+               for _ in range(40)]
+    # grid points and midpoints of E2M1 at scale 1 (ties at g = 1)
+    blocks.append(O.f32_to_bf16_rne(np.array([6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -1.25,
+                                              -1.75, -2.5, -3.5, -5, 0], np.float32)))
+    x = np.stack(blocks)
+    for g in (1.0, O.global_scale(x), 0.0123456789, 3.7e-3):
+        _assert_quantize_matches_exact_steps(x, g)
+
+
+def test_quantize_scale_order_at_e4m3_midpoints():
+    # Global scales g for which (amax / 6) / g, each division rounded, is exactly a
+    # midpoint between two E4M3 values while amax / (6 g) falls on the other side of
+    # it: the scale byte then depends on the order of the two divisions, so these
+    # blocks separate the stated order from a one-division shortcut.  (amax = 6.375,
+    # amax / 6 = 1.0625 exactly; the scales are searched over float32 neighbours.)
+    e4 = np.array([float(v) for v in _e4m3_values()])
+    found = []
+    for b in range(0x30, 0x58):
+        mid = (e4[b] + e4[b + 1]) / 2
+        g0 = np.float32(1.0625 / mid)
+        g = (g0 + np.arange(-3000, 3000, dtype=np.float32) * np.spacing(g0)).astype(np.float32)
+        s = (np.float32(1.0625) / g).astype(np.float32)
+        sw = (np.float32(6.375) / (np.float32(6.0) * g).astype(np.float32)).astype(np.float32)
+        ok = (s.astype(np.float64) == mid) & (np.sign(sw.astype(np.float64) - mid) != 0)
+        if ok.any():
+            found.append(float(g[np.flatnonzero(ok)[0]]))
+    assert len(found) >= 4
+    rng = np.random.default_rng(13)
+    for g in found:
+        vals = np.concatenate([[6.375], rng.uniform(-6, 6, 15)]).astype(np.float32)
+        _assert_quantize_matches_exact_steps(O.f32_to_bf16_rne(vals)[None, :], g)
+
+
+def test_quantize_f32_rounds_the_quotient_in_float32():
+    # Float32 inputs (the residual of the two-pass quantiser) can put x / denom within
+    # half an ulp of an E2M1 midpoint without reaching it, so the float32 rounding of
+    # the denominator and of the quotient decide codes.  The blocks hold, besides their
+    # amax (6 times the denominator), the seventeen float32 neighbours of
+    # midpoint x denominator for every E2M1 midpoint, under several global scales.
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    e4 = np.array([float(v) for v in _e4m3_values()])
+    n_ties = 0
+    for g in (0.7, 0.0123456789, 1.1, 3.3e-3, 0.3):
+        g32 = np.float32(g)
+        s = np.float32(np.float32(np.float32(6.0) / np.float32(6.0)) / g32)
+        sbyte = int(O.e4m3_encode_rne_satfinite(np.array([s], np.float32))[0])
+        d = np.float32(np.float32(e4[sbyte]) * g32)
+        xs = []
+        for m in mids:
+            base = np.float32(m * float(d))
+            for k in range(-8, 9):
+                x = np.float32(base + np.float32(k) * np.spacing(base))
+                q = Fraction(float(x)) / Fraction(float(d))
+                n_ties += int(q != m and _rn_f32(q) == m)
+                xs.append(x)
+        xs = np.array(xs, np.float32)
+        blocks = []
+        for c in range(0, len(xs), 15):
+            chunk = xs[c:c + 15]
+            blk = np.zeros(16, np.float32)
+            blk[0] = np.float32(6.0 * float(d))
+            blk[1:1 + len(chunk)] = chunk
+            blocks.append(blk)
+        _assert_quantize_matches_exact_steps(np.stack(blocks), g, f32=True)
+    assert n_ties >= 10  # quotients that round onto a midpoint without equalling it
+
+
+def test_residual_equals_exact_rational_steps():
+    # r = RN(x - RN(value * scale * g)), value * scale exact: checked element by element
+    # with exact rationals and the hand-written float32 rounding, on N(0,1) data whose
+    # global scale is not a power of two (so RN(value * scale * g) does round).
+    x = G.bf16_normal(4, 256, 31, "x")
+    g = O.global_scale(x)
+    codes, sf = O.quantize(x, g)
+    r = O.residual_f32(x, codes, sf, g)
+    gf = Fraction(float(np.float32(g)))
+    e4 = _e4m3_values()
+    cu = O.unpack_codes(codes)
+    xf = O.bf16_bits_to_f64(x)
+    for i in range(x.shape[0]):
+        for k in range(x.shape[1]):
+            val = _e2m1_from_bits(int(cu[i, k]))
+            want = _rn_f32(Fraction(float(xf[i, k])) - _rn_f32(val * e4[int(sf[i, k // 16])] * gf))
+            assert Fraction(float(r[i, k])) == want, (i, k)
