@@ -170,10 +170,18 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """Hash of the pair kernel's code (its file and the PTX helpers), comments and
+    whitespace removed: the committed counters stay valid across comment edits and
+    are dropped by any change to the code itself."""
+    import re
+
     h = hashlib.sha256()
     for name in ("gemm_w4a4.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "nvfp4_block_scaled_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "nvfp4_block_scaled_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
