@@ -15,10 +15,14 @@
 //               round-to-nearest-even to BF16, stores to D.
 // Tiles are 128 x BN (BN = 128 or 256) per CTA; a persistent grid walks them in a
 // grouped raster so that a wave shares A rows and B columns in L2.  Large shapes run
-// the CTA-pair kernel (256 x 256 tiles); shapes with few tiles split K over a
-// thread block cluster (the split-K kernel).  Every kernel supports programmatic
-// dependent launch: its producer streams the first weight (B) stages before it
-// waits for the previous grid in the stream, and loads A only after.
+// the CTA-pair kernel (256 x 256 tiles), optionally with a stream-K schedule over a
+// caller workspace; shapes with few tiles split K over a thread block cluster (the
+// split-K kernel).  Every kernel supports programmatic dependent launch: its
+// producer streams the first weight (B) stages before it waits for the previous
+// grid in the stream, and loads A only after.  Every kernel also takes b_shift: with
+// 1, A holds 2K codes (the two-pass activation, value and residual K-blocks
+// interleaved) and A's K-block kb meets B's K-block kb >> 1, so both passes
+// accumulate into one tile while the weight is read once.
 
 #include <cuda_bf16.h>
 
@@ -589,8 +593,11 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // here) and commit to an "sf" barrier; the leader's MMA thread waits for both,
 // issues the stage's four MMAs and releases the stage to both CTAs with a multicast
 // commit.  Eight epilogue warps per CTA drain the accumulator (128 lanes x 256
-// columns) into a 128-byte-swizzled BF16 staging tile, release the accumulator,
-// and write D with TMA stores.
+// columns) into a 128-byte-swizzled BF16 staging tile, loading the next 32-column
+// chunk from TMEM while converting the current one; the accumulator is released as
+// soon as the last chunk is in registers (it is single-buffered: two 256-column
+// accumulators would leave no TMEM columns for the scale slots), and D goes out
+// with TMA stores.
 namespace pair {
 
 constexpr int kStages = 4;
