@@ -157,18 +157,18 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
 // Fused quantize + pack.  One thread block of 16 warps per (128-row band, 2 atoms
 // = 8 scale columns): lane l of a warp takes scale column 8*tile + l%8 of row
 // 4*(16*rr + w) + l/8 (rr = 0, 1), so a warp quantises four rows per step, reading
-// 256 contiguous bytes of each.  Two shuffles assemble each 4-scale word of an atom
-// into a shared-memory tile, which is then written atom by atom, 512 contiguous
-// bytes each (word w of an atom holds row 32*(w%4) + w/4): scattered single-byte
-// scale stores in the layout cost more than the separate packing pass.  Small tiles
-// keep the last wave short: 8192 x 5120 is 2560 tiles for 304 resident blocks (with
-// 8-atom tiles, 640 tiles took three rounds where 2.1 would do).  Rows past `rows`
-// and scale columns past C give zero scale bytes and no codes.  (16 warps per block:
-// the quantiser is bound by its arithmetic, so it wants the SM's full 64 warps.)
+// 256 contiguous bytes of each.  Two shuffles assemble each 4-scale word (one row's
+// scales of one atom) in the lane of its first column, which stores it at its place
+// in the packed layout (word 4*(r%32) + r/32 of the atom for row r of the band):
+// every word of the tile's atoms is written exactly once, padding rows and padding
+// columns as zero, with no shared-memory staging and no block barrier.  Small tiles
+// keep the last wave short (8192 x 5120 is 2560 tiles for about 304 resident blocks).
+// Rows past `rows` and scale columns past C give zero scale bytes and no codes.
+// (16 warps per block: the quantiser is bound by its arithmetic, so it wants the
+// SM's full 64 warps.)
 constexpr int kQPAtoms = 2;
 constexpr int kQPCols = 4 * kQPAtoms;        // scale columns per tile = lanes per row
 constexpr int kQPRowsPerWarp = 32 / kQPCols; // rows per warp and step
-constexpr int kQPPitch = kQPAtoms + 1;       // words per tile row (odd: spreads the banks)
 constexpr int kQPThreads = 512;
 static_assert(32 % kQPCols == 0, "a warp covers whole rows of a tile");
 
@@ -177,7 +177,6 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
                                                                      int64_t num_tiles, float g,
                                                                      uint2* __restrict__ codes,
                                                                      uint32_t* __restrict__ sf_packed) {
-  __shared__ uint32_t tile[128 * kQPPitch];
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -186,9 +185,9 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
   for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
     const int64_t band = t / tiles_per_band;
     const int64_t a0 = (t - band * tiles_per_band) * kQPAtoms;
-    const int na = static_cast<int>(groups - a0 < kQPAtoms ? groups - a0 : kQPAtoms);
     const int64_t c = 4 * a0 + col;
     const bool col_ok = c < C;
+    const bool atom_ok = a0 + (col >> 2) < groups;
 #pragma unroll
     for (int rr = 0; rr < 128 / (kWarps * kQPRowsPerWarp); ++rr) {
       const int row = (rr * kWarps + warp) * kQPRowsPerWarp + rsub;
@@ -202,15 +201,9 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
       }
       const uint32_t w1 = sbyte | (__shfl_down_sync(0xffffffffu, sbyte, 1) << 8);
       const uint32_t w2 = w1 | (__shfl_down_sync(0xffffffffu, w1, 2) << 16);
-      if ((col & 3) == 0) tile[row * kQPPitch + (col >> 2)] = w2;
+      if ((col & 3) == 0 && atom_ok)
+        sf_packed[(band * groups + a0 + (col >> 2)) * 128 + 4 * (row & 31) + (row >> 5)] = w2;
     }
-    __syncthreads();
-    uint32_t* dst = sf_packed + (band * groups + a0) * 128;
-    for (int i = threadIdx.x; i < na * 128; i += blockDim.x) {
-      const int a = i >> 7, wd = i & 127;
-      dst[i] = tile[(32 * (wd & 3) + (wd >> 2)) * kQPPitch + a];
-    }
-    __syncthreads();
   }
 }
 
