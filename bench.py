@@ -170,13 +170,13 @@ class ClockSampler:
 
 
 def kernel_source_hash():
-    """Hash of the pair kernel's code (its file and the PTX helpers), comments and
+    """Hash of the pair kernel's code (its file, its schedule and the PTX helpers), comments and
     whitespace removed: the committed counters stay valid across comment edits and
     are dropped by any change to the code itself."""
     import re
 
     h = hashlib.sha256()
-    for name in ("gemm_w4a4.cu", "ptx.cuh"):
+    for name in ("gemm_w4a4.cu", "pair_sched.h", "ptx.cuh"):
         with open(os.path.join(ROOT, "nvfp4_block_scaled_gb300", "csrc", name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
