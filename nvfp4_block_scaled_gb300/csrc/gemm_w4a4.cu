@@ -579,36 +579,50 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64 per instruction).  Each CTA
 // stages its own 128 rows of A and its own 128 rows of B.
 //
-// Operand delivery: under load a TMA copy takes about 1.4 us to land, so the
-// feed needs bytes in flight, and shared memory caps them.  Four stages of K = 256
-// keep three stages in flight while one is consumed; two stages of K = 512 (the
-// same bytes) measured 6-8 % slower at 8192^3 and 16384^3, and with four stages
-// loading only half of every B tile saves nothing: the feed no longer bounds the
-// kernel.  Per stage A and B arrive as one 16 KB box each (128 rows x 128 bytes,
-// 128-byte swizzle), the scale atoms as one SFA box (4 atoms, 2 KB) and one SFB box
-// (4 atoms of each of the tile's two bands, 4 KB).  All of both CTAs' copies
-// complete on the leader's "full" barrier.
+// Operand delivery: four stages of K = 256; per stage A and B arrive as one 16 KB
+// box each (128 rows x 128 bytes, 128-byte swizzle), the scale atoms as one SFA box
+// (4 atoms, 2 KB) and one SFB box (4 atoms of each of the tile's two bands, 4 KB).
+// All of both CTAs' copies complete on the leader's "full" barrier.
 //
-// Three scale warps of the leader move the atoms into the stage's TMEM slot with
-// tcgen05.cp (12 copies per 4 MMAs, the costly part of the tensor pipe's work
-// here) and commit to an "sf" barrier; the leader's MMA thread waits for both,
-// issues the stage's four MMAs and releases the stage to both CTAs with a multicast
-// commit.  Eight epilogue warps per CTA drain the accumulator (128 lanes x 256
-// columns) into a 128-byte-swizzled BF16 staging tile, loading the next 32-column
-// chunk from TMEM while converting the current one; the accumulator is released as
-// soon as the last chunk is in registers (it is single-buffered: two 256-column
-// accumulators would leave no TMEM columns for the scale slots), and D goes out
-// with TMA stores.
+// What bounds the tensor pipe here (measured on GB300 with MMA-only loops): one
+// 256 x 256 x 64 MMA occupies each SM of the pair for 128 cycles (16384 FP4 MACs per
+// SM per cycle, 4x the BF16 rate), and a stage needs 12 tcgen05.cp of 512-byte scale
+// atoms besides its 4 MMAs.  A tcgen05.cp blocks the warp that issues it for 64
+// cycles (about 128 while MMAs run), so one warp cannot issue a stage's copies in
+// the 512 cycles its MMAs take, and a thread that issues both copies and MMAs runs
+// at ~230 cycles per MMA.  So the copies are spread over six warps, placed on the
+// three sub-partitions that do not hold the MMA warp (one that shares it slows the
+// MMA issue), two copies per warp per stage.  They are ordered before the stage's
+// MMAs without waiting for their completion: each copy warp issues its copies,
+// executes tcgen05.fence::before_thread_sync and arrives on the stage's "sf"
+// barrier; the MMA thread waits for it and executes tcgen05.fence::after_thread_sync
+// before its MMAs, which places the MMAs after the copies in the tensor pipe.  The
+// MMA thread then issues the stage's four MMAs from precomputed descriptors and
+// releases the stage to both CTAs with a multicast commit.  Eight epilogue warps per
+// CTA drain the accumulator (128 lanes x 256 columns) into a 128-byte-swizzled BF16
+// staging tile, loading the next 32-column chunk from TMEM while converting the
+// current one; the accumulator is released as soon as the last chunk is in
+// registers (it is single-buffered: two 256-column accumulators would leave no TMEM
+// columns for the scale slots), and D goes out with TMA stores.
 namespace pair {
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kBKP = 256;                        // K per stage
 constexpr int kStepsP = kBKP / kMmaK;            // 4 MMAs per stage
 constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2;
 constexpr int kSFWarp = kFirstEpiWarp + kEpiWarps;  // first of the warps issuing the scale copies
-constexpr int kSFWarps = 3;                         // one per copy stream: SFA, SFB band 0, SFB band 1
-constexpr int kThreads = 32 * (kSFWarp + kSFWarps);
+constexpr int kSFWarps = 6;                         // warps 10, 11, 12, 14, 15, 16 (not sub-partition 1)
+constexpr int kSFCopies = 3 * kStepsP;              // per stage: SFA, SFB band 0, SFB band 1 per MMA
+constexpr int kAWarp = kSFWarp + kSFWarps + (kSFWarps - 1) / 3 + 1;  // 18: the A producer (sub-partition 2)
+constexpr int kNumWarps = kAWarp + 1;
+constexpr int kThreads = 32 * kNumWarps;
+// Copy-warp index of warp `w` (>= kSFWarp): the warps whose id is 1 mod 4 share the
+// MMA warp's sub-partition and issue no copies (-1).
+__host__ __device__ constexpr int sf_warp_index(int w) {
+  return (w & 3) == 1 ? -1 : w - kSFWarp - (w - kSFWarp) / 4;
+}
+static_assert(sf_warp_index(kAWarp - 2) == kSFWarps - 1 && (kAWarp & 3) == 2, "warp roles");
 constexpr int kABytes = 128 * (kBKP / 2);        // 16 KB: 128 rows x 128 B
 constexpr int kBBytes = 128 * (kBKP / 2);        // 16 KB
 constexpr int kSubTile = 128 * 128;              // 16 KB
@@ -619,9 +633,9 @@ constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
 constexpr int kOffSFA = kOffB + kStages * kBBytes;
 constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
-constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 4 boxes of 128 rows x 128 B (64 bf16 columns)
+constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 2 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
-constexpr int kOffBar = kOffOut + 4 * kOutBox;
+constexpr int kOffBar = kOffOut + 2 * kOutBox;
 constexpr int kNumBars = 3 * kStages + 4;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -720,21 +734,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nseg = sched.count();
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
+    // ------------------------------------------------------------ TMA producer of B (both CTAs)
+    // Issuing a tiled TMA load takes the issuing thread ~140 cycles, so one thread
+    // cannot issue a stage's four loads in the 512 cycles its MMAs take: this warp
+    // issues the weight side (B, SFB) and arms the stage's full barrier, warp kAWarp
+    // the activation side (A, SFA).  The weight loads may be issued before the
+    // previous grid in the stream has completed (programmatic launch).
     if (lane == 0) {
       const uint32_t full_leader = map_to_rank(bar_full, 0);
+      // The operands (A, B and their scales, read by many tiles) are kept in L2 ahead
+      // of D, which streams out once.
+      const uint64_t keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      // B first, A after the grid dependency (see gemm_nvf4_kernel).
-      DeferredA<kStages> dfr;
-      auto load_a = [&](int st, int kb, int mt, int) {
-        const uint32_t fb = full_leader + 8 * st;
-        tma_load_3d_pair(sbase + kOffA + st * kABytes, &tmA, fb, 0, mt * 256 + static_cast<int>(rank) * 128,
-                         (kBKP / 256) * kb);
-        tma_load_3d_pair(sbase + kOffSFA + st * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
-                         mt * 2 + static_cast<int>(rank));
-      };
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
@@ -742,17 +755,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int b_row = nt * 256 + static_cast<int>(rank) * 128;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (dfr.full()) dfr.flush(load_a);
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_spin(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
           const uint32_t fb = full_leader + 8 * stage;
-          tma_load_3d_pair(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * (kb >> b_shift));
-          tma_load_3d_pair(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, (kb >> b_shift) * kStepsP, nt * 2);
-          if (dfr.done) load_a(stage, kb, mt, 0); else dfr.add(stage, kb, mt, 0);
+          tma_load_3d_pair_hint(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * (kb >> b_shift),
+                                keep);
+          tma_load_3d_pair_hint(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, (kb >> b_shift) * kStepsP,
+                                nt * 2, keep);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (!dfr.done) dfr.flush(load_a);
       // Drain: wait until every stage has been released once more, so that no commit
       // arrival (and no copy of this CTA) is still in flight when the CTA exits.
       for (int i = 0; i < kStages && !*abort_flag; ++i) {
@@ -763,10 +775,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kStages; ++i) mbar_wait_for(bar_full + 8 * i, 0, 10000000ull);
       }
     }
+  } else if (warp == kAWarp) {
+    // ------------------------------------------------------------ TMA producer of A (both CTAs)
+    // The activations may be written by the previous grid in the stream: wait for it.
+    if (lane == 0) {
+      griddep_wait();
+      const uint32_t full_leader = map_to_rank(bar_full, 0);
+      const uint64_t keep = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int s = 0; s < nseg && ok; ++s) {
+        int t, kb0, kb1, kind;
+        sched.template seg<SK>(s, t, kb0, kb1, kind);
+        int mt, nt;
+        tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
+        const int a_row = mt * 256 + static_cast<int>(rank) * 128;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_spin(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t fb = full_leader + 8 * stage;
+          tma_load_3d_pair_hint(sbase + kOffA + stage * kABytes, &tmA, fb, 0, a_row, (kBKP / 256) * kb, keep);
+          tma_load_3d_pair_hint(sbase + kOffSFA + stage * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
+                                mt * 2 + static_cast<int>(rank), keep);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
     if (leader && lane == 0) {
       griddep_wait();  // time-limited waits start once the previous grid is done
+      // Descriptors of stage 0, K-step 0; stage s, K-step j adds s * 16 KB + j * 32 bytes
+      // to the start address (16-byte units in the low bits).
+      const uint64_t adesc0 = make_sdesc(sbase + kOffA, 16, 1024, 2);
+      const uint64_t bdesc0 = make_sdesc(sbase + kOffB, 16, 1024, 2);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -777,20 +819,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar_acce, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(bar_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          // The copy warps arrive only after the stage's operands landed (they wait
+          // for its full barrier) and their scale copies were issued.
+          if (!mbar_wait_spin(bar_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const int nk = min(kStepsP, KG - kb * kStepsP);
-          const uint32_t sfa_t = tmem + kTmemSF + stage * kSFSlotCols;
-          const uint32_t sfb_t = sfa_t + kSFACols;
-          const uint32_t sA = sbase + kOffA + stage * kABytes;
-          const uint32_t sB = sbase + kOffB + stage * kBBytes;
-          for (int j = 0; j < nk; ++j) {
-            const uint32_t koff = (j >> 2) * kSubTile + (j & 3) * (kMmaK / 2);
-            const uint64_t adesc = make_sdesc(sA + koff, 16, 1024, 2);
-            const uint64_t bdesc = make_sdesc(sB + koff, 16, 1024, 2);
-            tc_mma_nvf4_pair(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j,
-                             (kb != kb0 || j != 0) ? 1u : 0u);
+          const uint32_t sf_t = tmem + kTmemSF + stage * kSFSlotCols;
+          const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
+          if (KG - kb * kStepsP >= kStepsP) {
+            tc_mma_nvf4_pair(tmem, ad, bd, kIdesc, sf_t, sf_t + kSFACols, kb != kb0 ? 1u : 0u);
+#pragma unroll
+            for (int j = 1; j < kStepsP; ++j)
+              tc_mma_nvf4_pair(tmem, ad + 2 * j, bd + 2 * j, kIdesc, sf_t + 4 * j, sf_t + kSFACols + 8 * j, 1u);
+          } else {
+            const int nk = KG - kb * kStepsP;
+            for (int j = 0; j < nk; ++j)
+              tc_mma_nvf4_pair(tmem, ad + 2 * j, bd + 2 * j, kIdesc, sf_t + 4 * j, sf_t + kSFACols + 8 * j,
+                               (kb != kb0 || j != 0) ? 1u : 0u);
           }
           tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -803,14 +848,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kSFWarp) {
     // ------------------------------------------------------------ scale copies (leader CTA)
     // Move each landed stage's scale atoms into its TMEM slot (tcgen05.cp, both CTAs
-    // of the pair) and signal the MMA issuer.  Issued from their own threads, the
-    // copies overlap the previous stage's MMAs; spread over three warps (SFA, SFB band
-    // 0, SFB band 1), each on its own sub-partition, they overlap best: one warp was
-    // 5 % slower at 8192^3 and 16384^3, four or more (one sharing the MMA warp's
-    // sub-partition) far slower.  The slot is free: the stage only refills (and its
-    // full barrier only completes) after the MMAs that read the slot have committed.
-    const int stream = warp - kSFWarp;  // 0: SFA, 1: SFB band 0, 2: SFB band 1
-    if (leader && lane == 0) {
+    // of the pair) and signal the MMA issuer.  Copy c of a stage (0..11) is SFA of MMA
+    // c (c < 4) or band (c / 4 - 1) of SFB of MMA c % 4; warp i takes the copies with
+    // c % 6 == i.  The slot is free: the stage only refills (and its full barrier only
+    // completes) after the MMAs that read the slot have committed.
+    const int cw = sf_warp_index(warp);
+    if (leader && lane == 0 && cw >= 0) {
       griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
@@ -819,21 +862,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_spin(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nk = min(kStepsP, KG - kb * kStepsP);
-          const uint32_t sfa_t = tmem + kTmemSF + stage * kSFSlotCols;
-          const uint32_t sfb_t = sfa_t + kSFACols;
+          const uint32_t sf_t = tmem + kTmemSF + stage * kSFSlotCols;
           const uint32_t sSFA = sbase + kOffSFA + stage * kSFABytes;
           const uint32_t sSFB = sbase + kOffSFB + stage * kSFBBytes;
-          for (int j = 0; j < nk; ++j) {
-            if (stream == 0)
-              tc_cp_32x128b_warpx4_pair(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
-            else
-              tc_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4 * (stream - 1),
-                                        make_sdesc(sSFB + ((stream - 1) * kStepsP + j) * kAtom, 0, 128, 0));
+#pragma unroll
+          for (int c = cw; c < kSFCopies; c += kSFWarps) {
+            const int j = c % kStepsP, k = c / kStepsP;
+            if (j < nk) {
+              if (k == 0)
+                tc_cp_32x128b_warpx4_pair(sf_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+              else
+                tc_cp_32x128b_warpx4_pair(sf_t + kSFACols + 8 * j + 4 * (k - 1),
+                                          make_sdesc(sSFB + ((k - 1) * kStepsP + j) * kAtom, 0, 128, 0));
+            }
           }
-          tc_commit_pair_mc(bar_sf + 8 * stage, 0x1);
+          tc_fence_before();
+          mbar_arrive(bar_sf + 8 * stage);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -845,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (warp - kFirstEpiWarp) >> 2;     // column half (0: columns 0..127, 1: 128..255)
     const uint32_t acce_leader = map_to_rank(bar_acce, 0);
     const uint32_t out_base = sbase + kOffOut;
+    const uint64_t stream_out = policy_evict_first();
     const int r = q * 32 + lane;                   // accumulator row = TMEM lane
     uint32_t acc_phase = 0;
     bool stored = false;
@@ -931,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + hq[i].w);
           }
         }
-        const uint32_t box = out_base + (2 * h + (c32 >> 1)) * kOutBox + r * 128;
+        const uint32_t box = out_base + h * kOutBox + r * 128;  // one box per column half, used twice
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int c = (c32 & 1) * 4 + cc;   // 16-byte chunk (8 columns) within the 128-byte box row
@@ -944,6 +992,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : "memory");
         }
       };
+      // The staging box of a column half holds 64 columns: the first two chunks go out
+      // with one TMA store while the last two are loaded, and are staged once that
+      // store has read the box.
+      const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
+      const uint32_t box_rows = out_base + h * kOutBox + q * 32 * 128;
       uint32_t va[32], vb[32];
       tc_ld_32x32b_x32(trow, va);
       tc_wait_ld(va);
@@ -952,22 +1005,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_wait_ld(vb);
       tc_ld_32x32b_x32(trow + 64, va);
       stage_chunk(vb, 1);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d_hint(&tmD, box_rows, nt * 256 + h * 128, row0, stream_out);
+        bulk_commit_group();
+      }
       tc_wait_ld(va);
       tc_ld_32x32b_x32(trow + 96, vb);
-      stage_chunk(va, 2);
       tc_wait_ld(vb);
       // Accumulator read out: hand it back to the MMA issuer.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce_leader);
+      if (lane == 0) {
+        mbar_arrive_cluster(acce_leader);
+        bulk_wait_group_read0();
+      }
+      __syncwarp();
+      stage_chunk(va, 2);
       stage_chunk(vb, 3);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
-          tma_store_2d(&tmD, out_base + (2 * h + hb) * kOutBox + q * 32 * 128, nt * 256 + h * 128 + hb * 64, row0);
+        tma_store_2d_hint(&tmD, box_rows, nt * 256 + h * 128 + 64, row0, stream_out);
         bulk_commit_group();
       }
       stored = true;
