@@ -45,11 +45,19 @@ def test_clock_summary_without_samples_or_numbers():
     assert out["sm_mhz"] is None and out["sm_max_mhz"] is None and out["reasons"] == []
 
 
-def test_traffic_is_reported_only_for_the_measured_code(monkeypatch):
+def test_traffic_is_reported_only_for_the_measured_code(tmp_path, monkeypatch):
+    # A profile keyed to the current code is reported; any code change drops it.
+    import json
+
     real = bench.kernel_source_hash()
-    assert bench.profiled_traffic("gemm_8192") is not None  # the committed counters match the code
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(
+        json.dumps({"gemm_8192": {"dram_bytes_per_launch": 123, "source_hash": real}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: real)
+    assert bench.profiled_traffic("gemm_8192") == 123
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
-    assert bench.profiled_traffic("gemm_8192") is None      # any code change drops them
+    assert bench.profiled_traffic("gemm_8192") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: real)
     assert bench.profiled_traffic("no_such_kernel") is None
 
