@@ -24,11 +24,19 @@
  *     stream) and never synchronises the host.  Calls on different streams may run
  *     concurrently.
  *   - Every kernel is launched with programmatic dependent launch allowed: a call
- *     may start (and stream its weight operand) while the previous kernel in the
- *     stream is still running, and waits for that kernel to complete before it
- *     reads activations or writes its output.  A caller's own kernel launched after
- *     one of these with programmatic stream serialization must likewise wait
- *     (griddepcontrol.wait / cudaGridDependencySynchronize) before reading the output.
+ *     may start while the previous kernel in the stream is still running, and waits
+ *     for that kernel to complete before it reads activations or writes its output.
+ *     The WEIGHT operands of nvfp4_gemm* (B, SFB) and of nvfp4_w4a16_linear* (Wprep)
+ *     are read without that wait, so that a layer's weights stream in while the
+ *     previous kernel finishes.  Weights must therefore not be written by a kernel
+ *     in the same stream that is still running when the call starts: a kernel that
+ *     signals programmatic completion early (griddepcontrol.launch_dependents).
+ *     Every kernel that does not, and every producer of this library (quantize,
+ *     pack_scales, w4a16_prepare and their variants signal their dependents only by
+ *     completing), may write the weights right before the call.  A caller's own
+ *     kernel launched after one of these calls with programmatic stream
+ *     serialization must wait (griddepcontrol.wait / cudaGridDependencySynchronize)
+ *     before reading the output.
  *   - Errors are returned as nvfp4_status; nothing aborts or throws.  Arguments are
  *     checked on the host; device data (codes, scales) is NOT validated: a NaN
  *     (0x7F/0xFF) or negative scale byte given to nvfp4_gemm gives undefined

@@ -628,7 +628,6 @@ constexpr int kBBytes = 128 * (kBKP / 2);        // 16 KB
 constexpr int kSubTile = 128 * 128;              // 16 KB
 constexpr int kSFABytes = kStepsP * kAtom;       // 2 KB
 constexpr int kSFBBytes = 2 * kStepsP * kAtom;   // 4 KB: [band][atom]
-constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
 constexpr int kOffSFA = kOffB + kStages * kBBytes;
@@ -636,7 +635,7 @@ constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
 constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 2 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
 constexpr int kOffBar = kOffOut + 2 * kOutBox;
-constexpr int kNumBars = 3 * kStages + 4;
+constexpr int kNumBars = 4 * kStages + 5;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
@@ -681,13 +680,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + kOffBar;             // both CTAs' copies (leader's copy is used)
+  const uint32_t bar_full = sbase + kOffBar;             // both CTAs' A and B bytes (leader's copy is used)
   const uint32_t bar_empty = bar_full + 8 * kStages;     // stage released by the MMAs (both CTAs)
   const uint32_t bar_accf = bar_empty + 8 * kStages;
   const uint32_t bar_acce = bar_accf + 8;
   const uint32_t bar_sf = bar_acce + 8;                 // stage's scales are in TMEM (leader)
   const uint32_t bar_pub = bar_sf + 8 * kStages;        // stream-K: this CTA's head partial is written
   const uint32_t bar_seen = bar_pub + 8;                // stream-K: the head partial of the tail is ready
+  const uint32_t bar_accl = bar_seen + 8;               // follower: its epilogue warps have read the accumulator
+  const uint32_t bar_fsf = bar_accl + 8;                // both CTAs' scale atoms of the stage (leader's copy)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
 
@@ -704,7 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
-    mbar_init(bar_acce, 2 * kEpiWarps);
+    mbar_init(bar_acce, kEpiWarps + 1);  // the leader's epilogue warps + one forwarded arrival
+    mbar_init(bar_accl, kEpiWarps);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar_fsf + 8 * s, 1);
     for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, kSFWarps);
     mbar_init(bar_pub, kEpiWarps);  // each used at most once per launch (phase 0)
     mbar_init(bar_seen, 1);
@@ -742,12 +745,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // previous grid in the stream has completed (programmatic launch).
     if (lane == 0) {
       const uint32_t full_leader = map_to_rank(bar_full, 0);
+      const uint32_t fsf_leader = map_to_rank(bar_fsf, 0);
       // The operands (A, B and their scales, read by many tiles) are kept in L2 ahead
       // of D, which streams out once.
       const uint64_t keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int issued = 0;
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
@@ -755,24 +760,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int b_row = nt * 256 + static_cast<int>(rank) * 128;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_spin(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
-          if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * kStageBytes);
-          const uint32_t fb = full_leader + 8 * stage;
-          tma_load_3d_pair_hint(sbase + kOffB + stage * kBBytes, &tmB, fb, 0, b_row, (kBKP / 256) * (kb >> b_shift),
-                                keep);
-          tma_load_3d_pair_hint(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fb, 0, (kb >> b_shift) * kStepsP,
-                                nt * 2, keep);
+          // The first kStages stages are free; the wait for the next one can only end
+          // after the MMAs, which wait for the previous grid: wait for it here too, so
+          // that the time limit counts from its completion.
+          if (++issued == kStages + 1) griddep_wait();
+          if (!mbar_wait_spin<true>(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          // The scale atoms complete on their own barrier and go first, so that the
+          // scale copies into TMEM overlap the arrival of the A and B tiles.
+          if (leader) {
+            mbar_arrive_expect_tx(bar_fsf + 8 * stage, 2 * (kSFABytes + kSFBBytes));
+            mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (kABytes + kBBytes));
+          }
+          tma_load_3d_pair_hint(sbase + kOffSFB + stage * kSFBBytes, &tmSFB, fsf_leader + 8 * stage, 0,
+                                (kb >> b_shift) * kStepsP, nt * 2, keep);
+          tma_load_3d_pair_hint(sbase + kOffB + stage * kBBytes, &tmB, full_leader + 8 * stage, 0, b_row,
+                                (kBKP / 256) * (kb >> b_shift), keep);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
       // Drain: wait until every stage has been released once more, so that no commit
       // arrival (and no copy of this CTA) is still in flight when the CTA exits.
+      if (issued <= kStages) griddep_wait();
       for (int i = 0; i < kStages && !*abort_flag; ++i) {
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag)) break;
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
       if (*abort_flag && leader) {
-        for (int i = 0; i < kStages; ++i) mbar_wait_for(bar_full + 8 * i, 0, 10000000ull);
+        for (int i = 0; i < kStages; ++i) {
+          mbar_wait_for(bar_full + 8 * i, 0, 10000000ull);
+          mbar_wait_for(bar_fsf + 8 * i, 0, 10000000ull);
+        }
       }
     }
   } else if (warp == kAWarp) {
@@ -781,6 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       griddep_wait();
       const uint32_t full_leader = map_to_rank(bar_full, 0);
+      const uint32_t fsf_leader = map_to_rank(bar_fsf, 0);
       const uint64_t keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -792,11 +810,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int a_row = mt * 256 + static_cast<int>(rank) * 128;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_spin(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
-          const uint32_t fb = full_leader + 8 * stage;
-          tma_load_3d_pair_hint(sbase + kOffA + stage * kABytes, &tmA, fb, 0, a_row, (kBKP / 256) * kb, keep);
-          tma_load_3d_pair_hint(sbase + kOffSFA + stage * kSFABytes, &tmSFA, fb, 0, kb * kStepsP,
+          if (!mbar_wait_spin<true>(bar_empty + 8 * stage, phase ^ 1, abort_flag)) { ok = false; break; }
+          tma_load_3d_pair_hint(sbase + kOffSFA + stage * kSFABytes, &tmSFA, fsf_leader + 8 * stage, 0, kb * kStepsP,
                                 mt * 2 + static_cast<int>(rank), keep);
+          tma_load_3d_pair_hint(sbase + kOffA + stage * kABytes, &tmA, full_leader + 8 * stage, 0, a_row,
+                                (kBKP / 256) * kb, keep);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -816,12 +834,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
-        if (!mbar_wait(bar_acce, acc_phase ^ 1, abort_flag)) break;
+        if (!mbar_wait_spin<true>(bar_acce, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
           // The copy warps arrive only after the stage's operands landed (they wait
           // for its full barrier) and their scale copies were issued.
           if (!mbar_wait_spin(bar_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_spin<true>(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sf_t = tmem + kTmemSF + stage * kSFSlotCols;
           const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
@@ -862,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_spin(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!mbar_wait_spin<true>(bar_fsf + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nk = min(kStepsP, KG - kb * kStepsP);
           const uint32_t sf_t = tmem + kTmemSF + stage * kSFSlotCols;
@@ -896,6 +915,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;                   // accumulator row = TMEM lane
     uint32_t acc_phase = 0;
     bool stored = false;
+    // Hand the accumulator back to the MMA issuer.  Arrivals from the other CTA of the
+    // cluster were measured to reach a waiting thread ~1.3 us late, so each of the
+    // leader's epilogue warps arrives locally, and the follower's warps arrive on a
+    // local barrier that one of them waits for before a single remote arrival.
+    uint32_t rel_phase = 0;
+    auto release_acc = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (leader) {
+        if (lane == 0) mbar_arrive(bar_acce);
+      } else {
+        if (lane == 0) mbar_arrive(bar_accl);
+        if (warp == kFirstEpiWarp && lane == 0 && mbar_wait_spin(bar_accl, rel_phase, abort_flag))
+          mbar_arrive_cluster(acce_leader);
+      }
+      rel_phase ^= 1;
+    };
     // Stream-K workspace slots: one 128 KB FP32 partial per (pair, rank) and one flag
     // each.  A slot is laid out in the epilogue's own register order, [warp][32-column
     // chunk][float4 i][lane], so that both the publishing and the finishing CTA (same
@@ -925,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) hp[i] = __ldcg(part + i * 32);
       }
-      if (!warp_wait(bar_accf, acc_phase, abort_flag)) break;
+      if (!warp_wait_spin<true>(bar_accf, acc_phase, abort_flag)) break;
       tc_fence_after();
       if (SK && kind == PairSched::kHead) {
         // ---- head piece: publish the FP32 partial tile for the pair that finishes it
@@ -943,9 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
         }
         // The accumulator is read out: hand it back before the stores drain.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acce_leader);
+        release_acc();
         __threadfence();  // this warp's stores are visible at GPU scope before its arrival
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pub);
@@ -1005,20 +1039,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_wait_ld(vb);
       tc_ld_32x32b_x32(trow + 64, va);
       stage_chunk(vb, 1);
+      tc_wait_ld(va);
+      tc_ld_32x32b_x32(trow + 96, vb);
+      tc_wait_ld(vb);
+      // Accumulator read out: hand it back to the MMA issuer (before any store of this
+      // tile is in flight: an arrival issued behind a TMA store was measured to reach
+      // its waiter ~1 us late).
+      release_acc();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         tma_store_2d_hint(&tmD, box_rows, nt * 256 + h * 128, row0, stream_out);
         bulk_commit_group();
-      }
-      tc_wait_ld(va);
-      tc_ld_32x32b_x32(trow + 96, vb);
-      tc_wait_ld(vb);
-      // Accumulator read out: hand it back to the MMA issuer.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_cluster(acce_leader);
         bulk_wait_group_read0();
       }
       __syncwarp();

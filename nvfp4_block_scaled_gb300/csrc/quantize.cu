@@ -143,8 +143,10 @@ __device__ __forceinline__ void residual_block(const float (&f)[16], uint32_t c0
 __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t nblocks,
                                                        float g, uint2* __restrict__ codes,
                                                        uint8_t* __restrict__ sf) {
-  griddep_wait();                // x may be produced by the previous grid in the stream
-  griddep_launch_dependents();   // a following GEMM may start streaming its weights
+  // x may be produced by the previous grid in the stream.  No early launch_dependents:
+  // a following GEMM or W4A16 call reads its weights before waiting for this grid, so
+  // this grid (which may be writing them) signals its dependents only by completing.
+  griddep_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
     uint32_t c0, c1;
@@ -177,8 +179,7 @@ __global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4
                                                                      int64_t num_tiles, float g,
                                                                      uint2* __restrict__ codes,
                                                                      uint32_t* __restrict__ sf_packed) {
-  griddep_wait();
-  griddep_launch_dependents();
+  griddep_wait();  // x from the previous grid; dependents are signalled at completion (see quantize_kernel)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = lane % kQPCols, rsub = lane / kQPCols;
   constexpr int kWarps = kQPThreads / 32;
@@ -226,8 +227,7 @@ __global__ void __launch_bounds__(kQPThreads) quantize_two_pass_kernel(const uin
                                                                        float g, uint2* __restrict__ codes,
                                                                        uint32_t* __restrict__ sf_packed) {
   __shared__ uint32_t tile[128 * kTPPitch];
-  griddep_wait();
-  griddep_launch_dependents();
+  griddep_wait();  // x from the previous grid; dependents are signalled at completion (see quantize_kernel)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = lane & 15, rsub = lane >> 4;
   constexpr int kWarps = kQPThreads / 32;
@@ -287,8 +287,7 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restr
                                                           int64_t num_tiles, bool word_loads,
                                                           uint32_t* __restrict__ out) {
   __shared__ uint32_t tile[128 * kPackPitch];
-  griddep_wait();
-  griddep_launch_dependents();
+  griddep_wait();  // x from the previous grid; dependents are signalled at completion (see quantize_kernel)
   for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
     const int64_t band = t / tiles_per_band;
     const int64_t g0 = (t - band * tiles_per_band) * kPackAtoms;

@@ -358,3 +358,39 @@ def test_gemm_streamk_rejects_bad_workspace():
     with pytest.raises(nv.NVFP4Error) as e:
         nv.gemm_streamk(a, sfa, b, sfb, 1.0, M, N, K, small)
     assert e.value.status == -1
+
+
+@pytest.mark.parametrize("M,N,K,config", [(1024, 2048, 4096, 3), (128, 5120, 5120, 0), (512, 1024, 2048, 1)])
+def test_weights_written_by_the_kernel_just_before(M, N, K, config):
+    # The GEMM reads its weight operand (B, SFB) before it waits for the previous
+    # kernel in the stream.  The library's producers signal their dependents only by
+    # completing, so weights they write immediately before the GEMM -- with nothing
+    # in between -- must be complete when the GEMM reads them.  Two producers:
+    # quantize_packed (codes and packed scales) and pack_scales (packed scales only).
+    x, w, gx, gw = _llm_operands(M, N, K, 23)
+    alpha = float(np.float32(gx) * np.float32(gw))
+    A, SFA = nv.quantize_packed(x, gx)
+    B = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+    SFB = torch.empty(nv.packed_scales_bytes(N, K), dtype=torch.uint8, device="cuda")
+    B_rm, SFB_rm = nv.quantize(w, gw)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    wh = G.bf16_normal(N, K, 23, "w", 0.02)
+    Bh, SFBh = O.quantize(wh, gw)
+    Ah, SFAh = O.quantize(G.bf16_normal(M, K, 23, "x"), gx)
+    want = None
+    for it in range(8):
+        B.zero_()
+        SFB.zero_()
+        D.zero_()
+        if it % 2 == 0:
+            nv.quantize_packed(w, gw, B, SFB)
+        else:
+            B.copy_(B_rm)
+            nv.pack_scales(SFB_rm, K, SFB)
+        nv.gemm(A, SFA, B, SFB, alpha, M, N, K, out=D, config=config)
+        torch.cuda.synchronize()
+        if want is None:
+            want = D.clone()
+            check_sampled(Ah, SFAh, Bh, SFBh, alpha, D, M, N, 512, f"weights just written {M}x{N}x{K}")
+        assert torch.equal(D.view(torch.int16), want.view(torch.int16)), f"iteration {it}"
+    assert nv.device_error() == 0

@@ -221,3 +221,33 @@ def test_linear_more_than_1024_tokens():
     torch.cuda.synchronize()
     ref, abs_sum = O.w4a16_linear(x, W, SW, 0.75)
     assert_within(host_f64(y), ref, abs_sum, 0.75, "w4a16 M=1300")
+
+
+@pytest.mark.parametrize("M", [1, 32, 144])
+def test_weights_prepared_by_the_kernel_just_before(M):
+    # The linear call streams its prepared weights before it waits for the previous
+    # kernel in the stream; w4a16_prepare signals its dependents only by completing,
+    # so a weight prepared immediately before the call (nothing in between) is read
+    # complete.  Every repetition must give the bits of the first, checked against
+    # the oracle.
+    N, K = 5120, 5120
+    W, SW, g = quantized_weight(N, K, 41)
+    x = G.bf16_normal(M, K, 41, "x")
+    xd, Wd, SWd = dev_bf16(x), dev(W), dev(SW)
+    wp = torch.empty(nv.w4a16_prepared_bytes(N, K), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    want = None
+    for it in range(8):
+        wp.zero_()
+        y.zero_()
+        nv.w4a16_prepare(Wd, SWd, out=wp)
+        nv.w4a16_linear(xd, wp, g, N, out=y)
+        torch.cuda.synchronize()
+        if want is None:
+            want = y.clone()
+            rows, cols = sample_points(M, N, 512)
+            ref, abs_sum = O.w4a16_linear_at(x, W, SW, g, rows, cols)
+            assert_within(host_f64(y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]),
+                          ref, abs_sum, g, "prepared just before")
+        assert torch.equal(y.view(torch.int16), want.view(torch.int16)), f"iteration {it}"
+    assert nv.device_error() == 0
