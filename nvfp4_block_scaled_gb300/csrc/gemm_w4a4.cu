@@ -635,7 +635,7 @@ constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
 constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 2 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
 constexpr int kOffBar = kOffOut + 2 * kOutBox;
-constexpr int kNumBars = 4 * kStages + 5;
+constexpr int kNumBars = 4 * kStages + 4;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
@@ -687,8 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_sf = bar_acce + 8;                 // stage's scales are in TMEM (leader)
   const uint32_t bar_pub = bar_sf + 8 * kStages;        // stream-K: this CTA's head partial is written
   const uint32_t bar_seen = bar_pub + 8;                // stream-K: the head partial of the tail is ready
-  const uint32_t bar_accl = bar_seen + 8;               // follower: its epilogue warps have read the accumulator
-  const uint32_t bar_fsf = bar_accl + 8;                // both CTAs' scale atoms of the stage (leader's copy)
+  const uint32_t bar_fsf = bar_seen + 8;                // both CTAs' scale atoms of the stage (leader's copy)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
 
@@ -705,8 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_accf, 1);
-    mbar_init(bar_acce, kEpiWarps + 1);  // the leader's epilogue warps + one forwarded arrival
-    mbar_init(bar_accl, kEpiWarps);
+    mbar_init(bar_acce, 2 * kEpiWarps);
     for (int s = 0; s < kStages; ++s) mbar_init(bar_fsf + 8 * s, 1);
     for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, kSFWarps);
     mbar_init(bar_pub, kEpiWarps);  // each used at most once per launch (phase 0)
@@ -915,22 +913,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q * 32 + lane;                   // accumulator row = TMEM lane
     uint32_t acc_phase = 0;
     bool stored = false;
-    // Hand the accumulator back to the MMA issuer.  Arrivals from the other CTA of the
-    // cluster were measured to reach a waiting thread ~1.3 us late, so each of the
-    // leader's epilogue warps arrives locally, and the follower's warps arrive on a
-    // local barrier that one of them waits for before a single remote arrival.
-    uint32_t rel_phase = 0;
+    // Hand the accumulator back to the MMA issuer (every warp's TMEM loads have
+    // completed: tcgen05.wait::ld).  The follower's warps arrive with relaxed
+    // semantics: an arrival with release semantics at cluster scope waited ~700 ns
+    // (measured) for the SM's memory traffic in flight, while the accumulator's
+    // values are already in registers and nothing else needs ordering.
     auto release_acc = [&]() {
       tc_fence_before();
       __syncwarp();
-      if (leader) {
-        if (lane == 0) mbar_arrive(bar_acce);
-      } else {
-        if (lane == 0) mbar_arrive(bar_accl);
-        if (warp == kFirstEpiWarp && lane == 0 && mbar_wait_spin(bar_accl, rel_phase, abort_flag))
-          mbar_arrive_cluster(acce_leader);
+      if (lane == 0) {
+        if (leader) mbar_arrive(bar_acce);
+        else mbar_arrive_relaxed_cluster(acce_leader);
       }
-      rel_phase ^= 1;
     };
     // Stream-K workspace slots: one 128 KB FP32 partial per (pair, rank) and one flag
     // each.  A slot is laid out in the epilogue's own register order, [warp][32-column

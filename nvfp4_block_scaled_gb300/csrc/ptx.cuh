@@ -381,6 +381,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive (relaxed, cluster scope) on an mbarrier given by its shared::cluster address:
+// no ordering of this thread's earlier memory operations.
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 2-D tiled TMA load into this CTA's shared memory for a CTA pair: completion is
 // signalled on the mbarrier at shared::cluster address `bar`, which may belong to
 // the peer CTA of the pair.
