@@ -269,6 +269,48 @@ def test_global_scale_reading():
     assert O.global_scale(np.zeros((2, 32), dtype=np.uint16)) == 1.0
 
 
+def test_global_scale_golden_values():
+    # Reading Q1: g = amax / (6 * 448), the largest E2M1 value times the largest
+    # E4M3 scale, rounded once to float32; amax is taken over magnitudes.  Hand-worked
+    # cases: 2688 = 6 * 448 gives exactly 1; a negative element of magnitude 5376 gives
+    # exactly 2; amax = 1 and 0.75 give 1/2688 and 3/10752 rounded to nearest float32
+    # (computed here from the exact rationals, not by a float division).
+    cases = [
+        ([2688.0, -1.0, 0.5], Fraction(1)),
+        ([1.0, -5376.0, 3.0], Fraction(2)),
+        ([1.0, -0.5, 0.25], _rn_f32(Fraction(1, 2688))),
+        ([-0.75, 0.5], _rn_f32(Fraction(3, 4) / 2688)),
+        ([float(255 * 2 ** 120), 1.0], _rn_f32(Fraction(255 * 2 ** 120, 2688))),  # the largest finite bf16
+    ]
+    for vals, want in cases:
+        bits = _bf16_bits_of(vals)
+        g = O.global_scale(bits.reshape(1, -1))
+        assert Fraction(g) == want, (vals, g, float(want))
+    assert _rn_f32(Fraction(1, 2688)) != Fraction(1, 2688)  # the rounding is not trivial
+
+
+def test_float64_gemm_is_exact_where_its_bound_holds_on_llm_scales():
+    # The LLM-shaped operands (quantised N(0,1) activations, N(0, 0.02) weights) carry
+    # block scales up to 448, so a product can reach 2^57 units of 2^-20 and float64
+    # accumulation is not exact in general.  Where an output's sum of |a_k b_k| stays
+    # below 2^53 units, every partial sum is an integer number of units below 2^53 and
+    # float64 must equal the exact int64 sum; the outputs outside the bound are
+    # counted and must be within the float64 rounding bound K * 2^-53 * sum|a b|.
+    for M, N, K in ((24, 40, 1024), (4, 8, 17408)):
+        x = G.bf16_normal(M, K, 7, "x")
+        w = G.bf16_normal(N, K, 7, "w", 0.02)
+        A, SFA = O.quantize(x, O.global_scale(x))
+        B, SFB = O.quantize(w, O.global_scale(w))
+        ref, abs_sum = O.gemm(A, SFA, B, SFB, 1.0)
+        units = O.gemm_exact_units(A, SFA, B, SFB)
+        exact = units.astype(np.float64) * 2.0 ** -20
+        in_bound = abs_sum * 2.0 ** 20 < 2.0 ** 53 * (1 - 2.0 ** -40)
+        assert np.array_equal(ref[in_bound], exact[in_bound])
+        out = ~in_bound
+        assert np.all(np.abs(ref[out] - exact[out]) <= K * 2.0 ** -53 * abs_sum[out])
+        print(f"K={K}: float64 exactness bound holds for {int(in_bound.sum())}/{in_bound.size} outputs")
+
+
 # ---------------------------------------------------------------- W4A16
 
 def test_w4a16_prepared_size_golden():
