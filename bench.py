@@ -588,14 +588,25 @@ def cpu_baseline_gemm(S, target_s=12.0, max_samples=1 << 16):
         total += n
         n = min(2 * n, 4096)
     tflops = total * 2 * S / elapsed / 1e12
+    affinity = len(os.sched_getaffinity(0))
     try:
         from threadpoolctl import threadpool_info
 
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        blas = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except ImportError:
-        cores = len(os.sched_getaffinity(0))
-    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{total} sampled outputs of the {S}^3 GEMM (full K={S} dot products, float64), {elapsed:.1f} s"}
+        blas = affinity
+    # Full-output oracle timings of the small square workloads (every output, float64).
+    full = {}
+    for Sf in (256, 2048):
+        Af, SFAf, Bf, SFBf = G.gemm_square_inputs(Sf, Sf, Sf, seed=0)
+        t0 = time.perf_counter()
+        O.gemm(Af, SFAf, Bf, SFBf, alpha)
+        dt = time.perf_counter() - t0
+        full[str(Sf)] = {"s": round(dt, 4), "GFLOP/s": round(2 * Sf ** 3 / dt / 1e9, 2)}
+    return {"value": tflops, "unit": "TFLOP/s", "cores": min(blas, affinity), "affinity_cores": affinity,
+            "blas_threads": blas, "kind": "oracle",
+            "sample": f"{total} sampled outputs of the {S}^3 GEMM (full K={S} dot products, float64), {elapsed:.1f} s",
+            "full_output": full}
 
 
 def run_ours(args):

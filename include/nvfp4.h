@@ -73,8 +73,9 @@ typedef enum {
   NVFP4_ERR_TIMEOUT = -6            /* a kernel gave up a bounded wait (see nvfp4_device_error) */
 } nvfp4_status;
 
-/* Static, human-readable name of a status code (never NULL). */
-const char* nvfp4_status_string(int status);
+/* Static, human-readable name of a status code (never NULL; values outside the enum
+   give "NVFP4_ERR_UNKNOWN"). */
+const char* nvfp4_status_string(nvfp4_status status);
 
 /* ABI version of this header: major * 10000 + minor * 100 + patch. */
 int nvfp4_version(void);
@@ -249,7 +250,10 @@ size_t nvfp4_gemm_streamk_workspace_bytes(void);
  *
  * There is one array per device, shared by every call on it: calls that overlap on
  * the GPU (other streams, other host threads) race on it and give wrong results or
- * time out.  Calls on one stream never overlap.
+ * time out.  Calls on one stream never overlap.  The array's address and the
+ * "already cleared" state are cached per device for the life of the process, so the
+ * entry point is not valid across cudaDeviceReset (or any other teardown of the
+ * device's primary context): after one, the cached address may be stale.
  * Errors as nvfp4_gemm_streamk, plus NVFP4_ERR_UNSUPPORTED_DEVICE, before anything is
  * enqueued, when the device's CTA-pair grid needs more workspace than the array holds,
  * and NVFP4_ERR_CUDA when the array's address cannot be looked up.

@@ -148,8 +148,8 @@ inline cudaStream_t as_stream(nvfp4_stream_t s) { return reinterpret_cast<cudaSt
 
 extern "C" {
 
-const char* nvfp4_status_string(int status) {
-  switch (status) {
+const char* nvfp4_status_string(nvfp4_status status) {
+  switch (static_cast<int>(status)) {
     case NVFP4_OK: return "NVFP4_OK";
     case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
     case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE";

@@ -5,6 +5,8 @@
 // (with lazy module loading, the CUDA default) by the first call of this entry point.
 // Nothing here allocates: the array's device address is looked up once per device
 // with cudaGetSymbolAddress, and the call goes through nvfp4_gemm_streamk unchanged.
+// The address and the "cleared" flag are cached per device ordinal for the life of
+// the process: the entry point is not valid across cudaDeviceReset.
 
 #include <atomic>
 #include <cstdint>

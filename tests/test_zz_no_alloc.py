@@ -57,3 +57,30 @@ def test_noalloc_rejects_bad_arguments_like_the_workspace_entry():
     with pytest.raises(nv.NVFP4Error) as e:
         nv.gemm_streamk_noalloc(a, sfa, b, sfb, float("nan"), M, N, K)
     assert e.value.status == -1
+
+
+def test_noalloc_stream_k_result_matches_the_oracle():
+    # A 1024-token layer (80 tiles of 256 x 256 on about 76 CTA pairs): the stream-K
+    # split runs through the static array, so its bits differ from the data-parallel
+    # nvfp4_gemm somewhere (a different FP32 summation order on the shared tiles),
+    # and sampled outputs and the corner tiles are within the tolerance of the exact
+    # reference.
+    from gpu_util import assert_within, corner_tiles, host_f64, sample_points
+    from oracle import nvfp4_oracle as O
+
+    M, N, K = 1024, 5120, 5120
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=11)
+    a, sfa, b, sfb = dev(A), nv.pack_scales(dev(SFA), K), dev(B), nv.pack_scales(dev(SFB), K)
+    alpha = G.alpha_uniform(11)
+    D = nv.gemm_streamk_noalloc(a, sfa, b, sfb, alpha, M, N, K)
+    Ddp = nv.gemm(a, sfa, b, sfb, alpha, M, N, K)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert not torch.equal(_bits(D), _bits(Ddp)), "the stream-K schedule did not run"
+    rows, cols = sample_points(M, N, 512)
+    ref, abs_sum = O.gemm_at(A, SFA, B, SFB, alpha, rows, cols)
+    assert_within(host_f64(D[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]), ref, abs_sum, alpha,
+                  "no-alloc stream-K samples")
+    for r0, r1, c0, c1 in corner_tiles(M, N):
+        ref, abs_sum = O.gemm_tile(A, SFA, B, SFB, alpha, r0, r1, c0, c1)
+        assert_within(host_f64(D[r0:r1, c0:c1]), ref, abs_sum, alpha, f"no-alloc tile {(r0, c0)}")
