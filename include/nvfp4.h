@@ -358,6 +358,26 @@ nvfp4_status nvfp4_w4a16_linear_colscale(const void* x_bf16, const void* Wprep, 
  */
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear);
 
+/*
+ * nvfp4_test_streamk_fault -- FOR TESTS ONLY: fault injection into the stream-K
+ * schedule of nvfp4_gemm_streamk / nvfp4_gemm_streamk_noalloc on the current device.
+ * No counterpart on the cited pages; it exists to exercise the timeout path without
+ * faulting, trapping or hanging the GPU.
+ *
+ *   skip_publish   nonzero: the pairs that start a shared tile (stream-K "heads")
+ *                  do not publish their partial, so the pairs that finish it wait on
+ *                  a flag that nothing sets; 0: normal operation.
+ *   flag_wait_ns   limit of those flag waits in nanoseconds (0 = the default 2 s).
+ *
+ * With skip_publish set, a launch that splits tiles ends (no hang) with
+ * nvfp4_device_error reporting NVFP4_ERR_TIMEOUT; its output is undefined.  Call
+ * again with (0, 0) to restore normal operation, then re-zero the stream-K workspace
+ * (or pass reset_scratch to nvfp4_gemm_streamk_noalloc) before the next stream-K call.
+ * Synchronous (device-global settings); not for use while stream-K launches run.
+ * Errors: NVFP4_ERR_UNSUPPORTED_DEVICE, NVFP4_ERR_CUDA.
+ */
+nvfp4_status nvfp4_test_streamk_fault(int skip_publish, uint64_t flag_wait_ns);
+
 #ifdef __cplusplus
 }
 #endif

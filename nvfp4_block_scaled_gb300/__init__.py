@@ -32,6 +32,7 @@ ABI_SYMBOLS = (
     "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_streamk_noalloc", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
     "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_device_error",
+    "nvfp4_test_streamk_fault",
 )
 
 NVFP4_OK = 0
@@ -79,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_w4a16_linear": (c_i, [c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_w4a16_linear_colscale": (c_i, [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_device_error": (c_i, [c_p, c_i]),
+        "nvfp4_test_streamk_fault": (c_i, [c_i, ctypes.c_uint64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -382,6 +384,12 @@ def w4a16_linear_colscale(x, Wprep, alpha_col, N: int, out=None, stream=None):
     _check("nvfp4_w4a16_linear_colscale", load_library().nvfp4_w4a16_linear_colscale(
         _ptr(x), _ptr(Wprep), _ptr(alpha_col), _ptr(out), M, int(N), K, _stream(stream)))
     return out
+
+
+def test_streamk_fault(skip_publish: bool, flag_wait_ns: int = 0) -> None:
+    """Tests only: make the stream-K flag waits run out (see nvfp4_test_streamk_fault)."""
+    _check("nvfp4_test_streamk_fault",
+           load_library().nvfp4_test_streamk_fault(1 if skip_publish else 0, int(flag_wait_ns)))
 
 
 def device_error(clear: bool = True, stream=None) -> int:

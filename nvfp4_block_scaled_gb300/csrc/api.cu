@@ -357,4 +357,11 @@ nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear) {
   return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_test_streamk_fault(int skip_publish, uint64_t flag_wait_ns) {
+  DeviceInfo dev;
+  const nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return gemm_test_streamk_fault(skip_publish, static_cast<unsigned long long>(flag_wait_ns));
+}
+
 }  // extern "C"

@@ -635,7 +635,7 @@ constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
 constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 2 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
 constexpr int kOffBar = kOffOut + 2 * kOutBox;
-constexpr int kNumBars = 4 * kStages + 4;
+constexpr int kNumBars = 4 * kStages + 5;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
@@ -653,15 +653,24 @@ constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(256 
 // The pair schedule is in pair_sched.h, shared with a host-side test.
 using ::nvfp4::sched::PairSched;
 
-// Bounded wait (2 s) for a stream-K flag to read 1 (acquire, GPU scope).
+// Fault injection for tests (off unless nvfp4_test_streamk_fault turns it on): the
+// head pairs of the stream-K schedule skip publishing their partials, and the flag
+// waits give up after g_flag_wait_ns, so that a test can make those waits run out and
+// check the timeout path without faulting or hanging anything.
+__device__ int g_test_skip_publish = 0;
+__device__ unsigned long long g_flag_wait_ns = kWaitLimitNs;
+
+// Bounded wait (2 s unless a test shortened it) for a stream-K flag to read 1
+// (acquire, GPU scope).
 __device__ __forceinline__ bool wait_flag(const uint32_t* flag, volatile int* abort) {
+  const uint64_t limit = g_flag_wait_ns;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
     if (v == 1u) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit) {
       *abort = 1;
       record_device_error(kDevErrTimeout);
       return false;
@@ -688,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_pub = bar_sf + 8 * kStages;        // stream-K: this CTA's head partial is written
   const uint32_t bar_seen = bar_pub + 8;                // stream-K: the head partial of the tail is ready
   const uint32_t bar_fsf = bar_seen + 8;                // both CTAs' scale atoms of the stage (leader's copy)
+  const uint32_t bar_drain = bar_fsf + 8 * kStages;     // every tcgen05 op of the launch has completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
 
@@ -706,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, 2 * kEpiWarps);
     for (int s = 0; s < kStages; ++s) mbar_init(bar_fsf + 8 * s, 1);
+    mbar_init(bar_drain, 1 + kSFWarps);  // the MMA thread and the copy warps, once each
     for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, kSFWarps);
     mbar_init(bar_pub, kEpiWarps);  // each used at most once per launch (phase 0)
     mbar_init(bar_seen, 1);
@@ -861,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit_pair_mc(bar_accf, 0x3);
         acc_phase ^= 1;
       }
+      tc_commit_pair_mc(bar_drain, 0x3);  // see the teardown
     }
   } else if (warp >= kSFWarp) {
     // ------------------------------------------------------------ scale copies (leader CTA)
@@ -901,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
+      tc_commit_pair_mc(bar_drain, 0x3);  // see the teardown
     }
   } else {
     // ------------------------------------------------------------ epilogue (8 warps, both CTAs)
@@ -977,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();  // this warp's stores are visible at GPU scope before its arrival
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pub);
-        if (warp == kFirstEpiWarp && lane == 0 && mbar_wait(bar_pub, 0, abort_flag)) {
+        if (warp == kFirstEpiWarp && lane == 0 && mbar_wait(bar_pub, 0, abort_flag) && !g_test_skip_publish) {
           __threadfence();
           asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + pair_id * 2 + rank), "r"(1u) : "memory");
         }
@@ -1063,6 +1076,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   }
 
+  // Before TMEM is released and the CTAs exit, every MMA and scale copy issued in this
+  // launch must have completed: the issuing threads' final commits arrive on both
+  // CTAs' drain barrier.  In a normal run the epilogue has already waited for the last
+  // MMAs; after a timed-out wait the roles stop early and this is what keeps the
+  // tensor pipe from writing freed TMEM or reading a departed CTA's shared memory.
+  if (threadIdx.x == 0) mbar_wait_for(bar_drain, 0, 200000000ull);
   tc_fence_before();
   cluster_sync_all();
   if (warp == 1) {
@@ -1306,6 +1325,14 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
 }
 
 }  // namespace
+
+nvfp4_status gemm_test_streamk_fault(int skip_publish, unsigned long long flag_wait_ns) {
+  const int skip = skip_publish != 0 ? 1 : 0;
+  const unsigned long long limit = flag_wait_ns != 0 ? flag_wait_ns : kWaitLimitNs;
+  if (cudaMemcpyToSymbol(pair::g_test_skip_publish, &skip, sizeof(skip)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaMemcpyToSymbol(pair::g_flag_wait_ns, &limit, sizeof(limit)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
 
 int read_device_error_gemm(bool clear) {
   int v = 0;

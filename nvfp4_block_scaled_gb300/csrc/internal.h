@@ -75,6 +75,8 @@ nvfp4_status encode_tmap_x_blocks(CUtensorMap* map, const void* x, int64_t M, in
 // Per-translation-unit device error words (see ptx.cuh): returns the recorded
 // status (0 if none) or NVFP4_ERR_CUDA, optionally clearing it.
 int read_device_error_gemm(bool clear);
+// Test-only fault injection for the stream-K schedule (see nvfp4_test_streamk_fault).
+nvfp4_status gemm_test_streamk_fault(int skip_publish, unsigned long long flag_wait_ns);
 int read_device_error_w4a16(bool clear);
 
 // Kernel launchers (defined next to their kernels).
