@@ -442,9 +442,19 @@ def w4a16_linear_at(x_bf16_bits, W, SW, alpha: float, rows, cols):
 #       a6 = (row g+8, k0+2t+8), a7 = (row g+8, k0+2t+9)
 #     bit positions of (code bit0, bit1, bit2, sign bit3):
 #       a0: 6, 7, 8, 15     a1: 22, 23, 24, 31
-#       a2: 3, 4, 5, 12     a3: 19, 20, 21, 28
-#       a4: 0, 1, 2, 9      a5: 16, 17, 18, 25
-#       a6: 10, 11, 13, 14  a7: 26, 27, 29, 30
+#       a2: 28, 29, 30, 5   a3: 12, 13, 14, 21
+#       a4: 25, 26, 27, 2   a5: 9, 10, 11, 18
+#       a6: 4, 0, 1, 3      a7: 20, 16, 17, 19
+#     With M = 0x81C081C0 (bits 6-8 and 15 of each bf16 half: mantissa MSB, the two
+#     low exponent bits, sign) the four bf16x2 fragment registers of a word are
+#       {a0, a1} = w & M,  {a2, a3} = rotl(w, 10) & M,  {a4, a5} = rotl(w, 13) & M,
+#       {a6, a7} = ((w & 0x001B001B) * 0x1084 mod 2^32) & M
+#     -- the product is the sum of the masked word shifted by 2, 7 and 12, three
+#     copies with no common bit, so no carries and the sum is their union.  Eight
+#     integer operations per word (one AND; rotate + AND twice; AND, multiply, AND).
+#     No choice of plain shifts or rotations covers all 32 bits with four copies of
+#     M (an exhaustive search finds none), which is why the fourth register takes
+#     the multiply.
 #   bytes [512 + 8 g, 512 + 8 g + 8) (shared by the four lanes with the same g):
 #     byte 2j = enc(scale(row g, block 4 kc + j)),
 #     byte 2j + 1 = enc(scale(row g + 8, block 4 kc + j)).
@@ -454,9 +464,9 @@ WPREP_BLOCK_BYTES = 576
 
 _CODE_BITS = (
     (6, 7, 8, 15), (22, 23, 24, 31),
-    (3, 4, 5, 12), (19, 20, 21, 28),
-    (0, 1, 2, 9), (16, 17, 18, 25),
-    (10, 11, 13, 14), (26, 27, 29, 30),
+    (28, 29, 30, 5), (12, 13, 14, 21),
+    (25, 26, 27, 2), (9, 10, 11, 18),
+    (4, 0, 1, 3), (20, 16, 17, 19),
 )
 # (row offset, k offset) of a0..a7 relative to (g, k0 + 2t)
 _CODE_POS = ((0, 0), (0, 1), (8, 0), (8, 1), (0, 8), (0, 9), (8, 8), (8, 9))

@@ -348,10 +348,11 @@ def _emulate_register_dequant(wprep, N, K):
                 sb = blk[512 + 8 * g:512 + 8 * g + 8]
                 for j in range(4):
                     w = int(words[j])
+                    rotl = lambda v, n: ((v << n) | (v >> (32 - n))) & 0xFFFFFFFF
                     r0 = w & mask
-                    r1 = (w << 3) & mask
-                    r2 = (w << 6) & mask
-                    r3 = (((w >> 4) & 0x00C000C0) | ((w >> 5) & 0x01000100) | ((w << 1) & 0x80008000))
+                    r1 = rotl(w, 10) & mask
+                    r2 = rotl(w, 13) & mask
+                    r3 = (((w & 0x001B001B) * 0x1084) & 0xFFFFFFFF) & mask
                     regs = (r0, r1, r2, r3)
                     srow = (int(sb[2 * j]), int(sb[2 * j + 1]))          # rows g, g+8
                     # reg -> (row offset, k offset of the low half)
