@@ -75,15 +75,18 @@ __global__ void __launch_bounds__(256) w4a16_prepare_kernel(const uint8_t* __res
       const uint32_t a2 = folded_code(W, SW, r1, k0, K), a3 = folded_code(W, SW, r1, k0 + 1, K);
       const uint32_t a4 = folded_code(W, SW, r0, k0 + 8, K), a5 = folded_code(W, SW, r0, k0 + 9, K);
       const uint32_t a6 = folded_code(W, SW, r1, k0 + 8, K), a7 = folded_code(W, SW, r1, k0 + 9, K);
+      // (magnitude bits 0-2, sign) of a0..a5 at (p, p+1, p+2, q); a6 and a7 at
+      // (4, 0, 1, 3) and (20, 16, 17, 19) -- the order dequant_word undoes.
       uint32_t w = 0;
       w |= ((a0 & 7u) << 6) | ((a0 >> 3) << 15);
       w |= ((a1 & 7u) << 22) | ((a1 >> 3) << 31);
-      w |= ((a2 & 7u) << 3) | ((a2 >> 3) << 12);
-      w |= ((a3 & 7u) << 19) | ((a3 >> 3) << 28);
-      w |= (a4 & 7u) | ((a4 >> 3) << 9);
-      w |= ((a5 & 7u) << 16) | ((a5 >> 3) << 25);
-      w |= ((a6 & 3u) << 10) | (((a6 >> 2) & 1u) << 13) | ((a6 >> 3) << 14);
-      w |= ((a7 & 3u) << 26) | (((a7 >> 2) & 1u) << 29) | ((a7 >> 3) << 30);
+      w |= ((a2 & 7u) << 28) | ((a2 >> 3) << 5);
+      w |= ((a3 & 7u) << 12) | ((a3 >> 3) << 21);
+      w |= ((a4 & 7u) << 25) | ((a4 >> 3) << 2);
+      w |= ((a5 & 7u) << 9) | ((a5 >> 3) << 18);
+      const uint32_t lo6 = ((a6 & 1u) << 4) | ((a6 >> 1) & 3u) | ((a6 >> 3) << 3);
+      const uint32_t lo7 = ((a7 & 1u) << 4) | ((a7 >> 1) & 3u) | ((a7 >> 3) << 3);
+      w |= lo6 | (lo7 << 16);
       words[j] = w;
     }
     uint8_t* dst = out + blk * kBlockBytes;
@@ -129,23 +132,28 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
 }
 
 // Dequantise one word (8 codes) into the 4 A-fragment registers, times the
-// row scales (s_lo for rows g, s_hi for rows g+8, both bf16x2 {s, s}).
+// row scales (s_lo for rows g, s_hi for rows g+8, both bf16x2 {s, s}).  The mask
+// keeps bits 6-8 and 15 of each half (mantissa MSB, the two low exponent bits,
+// sign): a code lands as the bf16 fp4 * 2^-126.  Registers 1 and 2 are rotations;
+// register 3 multiplies the masked word by 2^2 + 2^7 + 2^12, three copies that
+// share no bit, so the sum never carries.  8 integer operations per word.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_lo, uint32_t s_hi, uint32_t (&a)[4]) {
   constexpr uint32_t kMask = 0x81C081C0u;
   const uint32_t r0 = w & kMask;
-  const uint32_t r1 = (w << 3) & kMask;
-  const uint32_t r2 = (w << 6) & kMask;
-  const uint32_t r3 = ((w >> 4) & 0x00C000C0u) | ((w >> 5) & 0x01000100u) | ((w << 1) & 0x80008000u);
+  const uint32_t r1 = __funnelshift_l(w, w, 10) & kMask;
+  const uint32_t r2 = __funnelshift_l(w, w, 13) & kMask;
+  const uint32_t r3 = ((w & 0x001B001Bu) * 0x1084u) & kMask;
   a[0] = hmul2_bf16(r0, s_lo);
   a[1] = hmul2_bf16(r1, s_hi);
   a[2] = hmul2_bf16(r2, s_lo);
   a[3] = hmul2_bf16(r3, s_hi);
 }
 
-// bf16x2 {S, S} with S = 0x7000 | b << 4 for the scale byte b at byte index `idx` of `word`.
+// bf16x2 {S, S} with S = 0x7000 | b << 4 for the scale byte b at byte index `idx` of
+// `word`: one byte permute ({b, 0, b, 0}) and one multiply-add.
 __device__ __forceinline__ uint32_t scale_pair(uint32_t word, int idx) {
-  const uint32_t b = (word >> (8 * idx)) & 0xFFu;
-  return b * 0x00100010u + 0x70007000u;
+  const uint32_t v = __byte_perm(word, 0u, static_cast<uint32_t>(idx) * 0x0101u + 0x4040u);
+  return v * 16u + 0x70007000u;
 }
 
 constexpr int kDecodeNT = 8;                    // 16-row n-tiles per CTA (128 rows)
