@@ -330,7 +330,9 @@ W4A16_M = (1, 8, 32, 72, 144, 1024)
 
 
 def bench_w4a16(peaks, shapes=None):
-    """W4A16 decode: weight GB/s over CUDA-graph replay of rotated weight copies.
+    """W4A16 decode: weight GB/s over CUDA-graph replay of rotated weight copies, for
+    nvfp4_w4a16_linear and, up to 32 tokens, nvfp4_w4a16_linear_streamk (keys
+    prefixed streamk_).
     shapes: list of (N, K, [M...]); default every (N, K) of W4A16_NK with every M of W4A16_M."""
     import numpy as np
     import torch
@@ -349,53 +351,71 @@ def bench_w4a16(peaks, shapes=None):
         wbytes = nv.w4a16_prepared_bytes(N, K)
         copies = max(4, int(np.ceil(4 * l2 / wbytes)))
         ws = [w0.clone() for _ in range(copies)]
+        sk_ws = torch.zeros(nv.w4a16_streamk_workspace_bytes(), dtype=torch.uint8, device="cuda")
         for M in Ms:
             x = torch.from_numpy(G.bf16_normal(M, K, 0, "x").view(np.int16)).cuda().view(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-            for w in ws[:2]:
-                nv.w4a16_linear(x, w, 1.0, N, out=y)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            s = torch.cuda.Stream()
-            s.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(s):
-                with torch.cuda.graph(g, stream=s):
-                    for w in ws:
-                        nv.w4a16_linear(x, w, 1.0, N, out=y, stream=s)
-            torch.cuda.current_stream().wait_stream(s)
-            g.replay()
-            torch.cuda.synchronize()
-            best = None
-            for _ in range(3):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                g.replay()
-                e1.record()
-                torch.cuda.synchronize()
-                us = e0.elapsed_time(e1) * 1e3 / len(ws)
-                best = us if best is None else min(best, us)
-            # one call alone (weights not in L2, no call before or after it); a short
-            # device-side sleep queued first keeps the host's launch cost out of the
-            # event interval, so this is the call's device time
-            iso = []
-            for i in range(min(len(ws), 8)):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                torch.cuda.synchronize()
-                torch.cuda._sleep(200000)
-                e0.record()
-                nv.w4a16_linear(x, ws[i], 1.0, N, out=y)
-                e1.record()
-                torch.cuda.synchronize()
-                iso.append(e0.elapsed_time(e1) * 1e3)
             alg_bytes = wbytes + 2 * M * K + 2 * M * N
-            out[f"M{M}_N{N}_K{K}"] = {"us": round(best, 3), "weight_GBps": round(wbytes / best / 1e3, 1),
-                                      "GBps": round(alg_bytes / best / 1e3, 1),
-                                      "hbm_frac": round(alg_bytes / best / 1e3 / peaks["hbm_gbs"], 3),
-                                      "tflops": round(2 * M * N * K / best / 1e6, 1),
-                                      "isolated_us": round(statistics.median(iso), 2)}
-            del g
+            calls = {"": lambda w, s=None: nv.w4a16_linear(x, w, 1.0, N, out=y, stream=s)}
+            if M <= 32:
+                calls["streamk_"] = lambda w, s=None: nv.w4a16_linear_streamk(x, w, 1.0, N, sk_ws, out=y, stream=s)
+            cell = {}
+            for prefix, call in calls.items():
+                best, iso = _time_w4a16_call(call, ws)
+                cell.update({prefix + "us": round(best, 3), prefix + "weight_GBps": round(wbytes / best / 1e3, 1),
+                             prefix + "GBps": round(alg_bytes / best / 1e3, 1),
+                             prefix + "hbm_frac": round(alg_bytes / best / 1e3 / peaks["hbm_gbs"], 3),
+                             prefix + "tflops": round(2 * M * N * K / best / 1e6, 1),
+                             prefix + "isolated_us": round(iso, 2)})
+            out[f"M{M}_N{N}_K{K}"] = cell
         del ws
     return out
+
+
+def _time_w4a16_call(call, ws):
+    """(best per-call us over CUDA-graph replay of one call per weight copy, median
+    isolated us): the graph replays back to back three times; an isolated call has no
+    call before or after it and its weights are not in L2."""
+    import statistics as st
+
+    import torch
+
+    for w in ws[:2]:
+        call(w)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for w in ws:
+                call(w, s)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / len(ws)
+        best = us if best is None else min(best, us)
+    del g
+    # a short device-side sleep queued first keeps the host's launch cost out of the
+    # event interval, so the isolated number is the call's device time
+    iso = []
+    for i in range(min(len(ws), 8)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200000)
+        e0.record()
+        call(ws[i])
+        e1.record()
+        torch.cuda.synchronize()
+        iso.append(e0.elapsed_time(e1) * 1e3)
+    return best, st.median(iso)
 
 
 LLM_M = (128, 1024, 8192)

@@ -332,6 +332,47 @@ nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alp
                                 int64_t M, int64_t N, int64_t K, nvfp4_stream_t stream);
 
 /*
+ * Size in bytes of the workspace nvfp4_w4a16_linear_streamk needs on the current
+ * device (two FP32 partial slots of 32 tokens x 256 rows per SM plus two tickets per
+ * SM, about 64 KB per SM); 0 if no device can be queried.
+ */
+size_t nvfp4_w4a16_streamk_workspace_bytes(void);
+
+/*
+ * nvfp4_w4a16_linear_streamk -- nvfp4_w4a16_linear (or its per-column form) with the
+ * work split evenly over the SMs.
+ *
+ * [P2] Design, the persistent stream-K kernel: for up to 32 tokens one thread block
+ * per SM takes an equal contiguous share of the units (256 weight rows x 64 K) in
+ * row-group-major order, whatever N and K.  A row group split between blocks is
+ * summed through the workspace: each part stores its FP32 partial and takes a ticket,
+ * and the part that takes the last ticket adds all partials in part order (so the
+ * result does not depend on which part finishes last), writes y and zeroes the
+ * ticket.  No block waits for another.  More than 32 tokens run the tensor-core
+ * kernel of nvfp4_w4a16_linear (the workspace is not touched).
+ *
+ *   x_bf16, Wprep, y_bf16, M, N, K   as nvfp4_w4a16_linear.
+ *   alpha        the global scale, used when alpha_col is NULL (then finite).
+ *   alpha_col    NULL, or N FP32 per-output-column scales (16-byte aligned), as in
+ *                nvfp4_w4a16_linear_colscale; alpha is then ignored.
+ *   workspace    DEVICE buffer owned by the caller, at least
+ *                nvfp4_w4a16_streamk_workspace_bytes() bytes, 16-byte aligned,
+ *                zero-filled before its first use.  Every completed call leaves its
+ *                tickets at zero again, so the buffer needs no clearing between
+ *                calls (or CUDA-graph replays).  Calls that share a workspace must
+ *                not overlap in time; give concurrent streams their own.
+ *   workspace_bytes  its size.
+ * Errors as nvfp4_w4a16_linear, plus NVFP4_ERR_INVALID_ARG for a NULL or too small
+ * workspace.  After a call that reported a device error (nvfp4_device_error) the
+ * workspace must be zero-filled again.
+ * Accuracy as nvfp4_w4a16_linear.  Deterministic: repeated calls with the same
+ * shapes on the same device give bit-identical y (the split depends on the SM count).
+ */
+nvfp4_status nvfp4_w4a16_linear_streamk(const void* x_bf16, const void* Wprep, float alpha, const float* alpha_col,
+                                        void* y_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                        size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * nvfp4_w4a16_linear_colscale -- nvfp4_w4a16_linear with one FP32 weight scale per
  * output column instead of the global alpha:
  *

@@ -10,7 +10,8 @@ Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
   quantize, quantize_packed, quantize_two_pass, packed_scales_bytes, pack_scales,
   gemm, gemm_streamk, gemm_streamk_workspace_bytes, gemm_streamk_noalloc,
   gemm_two_pass, gemm_config_name, gemm_choose_config, w4a16_prepared_bytes,
-  w4a16_prepare, w4a16_linear, w4a16_linear_colscale, device_error.
+  w4a16_prepare, w4a16_linear, w4a16_linear_colscale, w4a16_streamk_workspace_bytes,
+  w4a16_linear_streamk, device_error.
 
 Every entry point checks that each tensor it is given holds at least the bytes the
 call reads or writes (the C ABI takes raw pointers and cannot), and raises
@@ -31,7 +32,8 @@ ABI_SYMBOLS = (
     "nvfp4_pack_scales", "nvfp4_gemm", "nvfp4_gemm_config", "nvfp4_gemm_streamk",
     "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_streamk_noalloc", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
-    "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_device_error",
+    "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_w4a16_streamk_workspace_bytes",
+    "nvfp4_w4a16_linear_streamk", "nvfp4_device_error",
     "nvfp4_test_streamk_fault",
 )
 
@@ -79,6 +81,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_w4a16_prepare": (c_i, [c_p, c_p, c_i64, c_i64, c_p, c_p]),
         "nvfp4_w4a16_linear": (c_i, [c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_w4a16_linear_colscale": (c_i, [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p]),
+        "nvfp4_w4a16_streamk_workspace_bytes": (ctypes.c_size_t, []),
+        "nvfp4_w4a16_linear_streamk": (c_i, [c_p, c_p, c_f, c_p, c_p, c_i64, c_i64, c_i64, c_p, ctypes.c_size_t,
+                                             c_p]),
         "nvfp4_device_error": (c_i, [c_p, c_i]),
         "nvfp4_test_streamk_fault": (c_i, [c_i, ctypes.c_uint64]),
     }
@@ -383,6 +388,34 @@ def w4a16_linear_colscale(x, Wprep, alpha_col, N: int, out=None, stream=None):
     _need(out, "out", 2 * M * int(N))
     _check("nvfp4_w4a16_linear_colscale", load_library().nvfp4_w4a16_linear_colscale(
         _ptr(x), _ptr(Wprep), _ptr(alpha_col), _ptr(out), M, int(N), K, _stream(stream)))
+    return out
+
+
+def w4a16_streamk_workspace_bytes() -> int:
+    return int(load_library().nvfp4_w4a16_streamk_workspace_bytes())
+
+
+def w4a16_linear_streamk(x, Wprep, alpha: float, N: int, workspace, alpha_col=None, out=None, stream=None):
+    """nvfp4_w4a16_linear_streamk: the decode work split evenly over the SMs; workspace
+    is a zero-filled uint8 device tensor of w4a16_streamk_workspace_bytes() bytes."""
+    import torch
+
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(Wprep, "Wprep", torch.uint8)
+    _cuda(workspace, "workspace", torch.uint8)
+    if alpha_col is not None:
+        _cuda(alpha_col, "alpha_col", torch.float32)
+        if alpha_col.numel() != N:
+            raise ValueError(f"alpha_col holds {alpha_col.numel()} scales, needs {N}")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda(out, "out", torch.bfloat16)
+    _need(Wprep, "Wprep", w4a16_prepared_bytes(int(N), K))
+    _need(out, "out", 2 * M * int(N))
+    _check("nvfp4_w4a16_linear_streamk", load_library().nvfp4_w4a16_linear_streamk(
+        _ptr(x), _ptr(Wprep), float(alpha), _ptr(alpha_col) if alpha_col is not None else None, _ptr(out), M,
+        int(N), K, _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

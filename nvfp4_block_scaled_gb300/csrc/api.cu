@@ -107,12 +107,13 @@ nvfp4_status encode_tmap_sf_3d(CUtensorMap* map, const void* base, int64_t rows,
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
-nvfp4_status encode_tmap_wprep(CUtensorMap* map, const void* wprep, int64_t N, int64_t K) {
+nvfp4_status encode_tmap_wprep(CUtensorMap* map, const void* wprep, int64_t N, int64_t K, uint32_t box_blocks,
+                               uint32_t box_ntiles) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return NVFP4_ERR_CUDA;
   const cuuint64_t dims[3] = {72, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(N / 16)};
   const cuuint64_t strides[2] = {576, static_cast<cuuint64_t>(K / 64) * 576};
-  const cuuint32_t box[3] = {72, 8, 8};
+  const cuuint32_t box[3] = {72, box_blocks, box_ntiles};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(wprep), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -345,6 +346,31 @@ nvfp4_status nvfp4_w4a16_linear_colscale(const void* x_bf16, const void* Wprep, 
   st = current_device(&dev);
   if (st != NVFP4_OK) return st;
   return launch_w4a16_linear(x_bf16, Wprep, 1.0f, alpha_col, y_bf16, M, N, K, as_stream(stream), dev);
+}
+
+size_t nvfp4_w4a16_streamk_workspace_bytes(void) {
+  DeviceInfo dev;
+  if (current_device(&dev) != NVFP4_OK) return 0;
+  return w4a16_streamk_workspace_bytes(dev);
+}
+
+nvfp4_status nvfp4_w4a16_linear_streamk(const void* x_bf16, const void* Wprep, float alpha, const float* alpha_col,
+                                        void* y_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                        size_t workspace_bytes, nvfp4_stream_t stream) {
+  nvfp4_status st = w4a16_checks(x_bf16, Wprep, y_bf16, M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (alpha_col == nullptr &&
+      (!(alpha == alpha) || alpha > 3.4028234663852886e38f || alpha < -3.4028234663852886e38f))
+    return NVFP4_ERR_INVALID_ARG;
+  if (alpha_col != nullptr && !aligned(alpha_col, 16)) return NVFP4_ERR_MISALIGNED;
+  if (workspace == nullptr) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return NVFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  if (workspace_bytes < w4a16_streamk_workspace_bytes(dev)) return NVFP4_ERR_INVALID_ARG;
+  return launch_w4a16_linear_streamk(x_bf16, Wprep, alpha_col != nullptr ? 1.0f : alpha, alpha_col, y_bf16, M, N,
+                                     K, workspace, as_stream(stream), dev);
 }
 
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear) {

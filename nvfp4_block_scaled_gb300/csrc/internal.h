@@ -65,8 +65,9 @@ nvfp4_status encode_tmap_sf_3d(CUtensorMap* map, const void* base, int64_t rows,
                                uint32_t box_bands);
 
 // 3-D UINT64 map over a prepared W4A16 weight viewed as [N/16][K/64][576 bytes];
-// a box is 8 n-tiles x 8 blocks (128 rows x 512 K, 36 KB).
-nvfp4_status encode_tmap_wprep(CUtensorMap* map, const void* wprep, int64_t N, int64_t K);
+// a box is box_ntiles n-tiles x box_blocks blocks (default 8 x 8: 128 rows x 512 K, 36 KB).
+nvfp4_status encode_tmap_wprep(CUtensorMap* map, const void* wprep, int64_t N, int64_t K, uint32_t box_blocks = 8,
+                               uint32_t box_ntiles = 8);
 // bf16 activations [M][K] viewed as [K/64 blocks][M tokens][64]: box = box_blocks x
 // box_rows tokens x 64, 128-byte swizzled; tokens past M read as zero.
 nvfp4_status encode_tmap_x_blocks(CUtensorMap* map, const void* x, int64_t M, int64_t K, uint32_t box_rows,
@@ -117,5 +118,11 @@ nvfp4_status launch_w4a16_prepare(const uint8_t* W, const uint8_t* SW, int64_t N
 // alpha_col: NULL for the global scale alpha, else N per-output-column FP32 scales.
 nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, const float* alpha_col, void* y,
                                  int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+// Balanced (stream-K) W4A16 linear: workspace bytes for the current device, and the
+// launch (more than 32 tokens go to launch_w4a16_linear's tensor-core kernel).
+size_t w4a16_streamk_workspace_bytes(const DeviceInfo& dev);
+nvfp4_status launch_w4a16_linear_streamk(const void* x, const void* Wprep, float alpha, const float* alpha_col,
+                                         void* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t stream,
+                                         const DeviceInfo& dev);
 
 }  // namespace nvfp4

@@ -107,12 +107,6 @@ __global__ void __launch_bounds__(256) w4a16_prepare_kernel(const uint8_t* __res
 
 // ------------------------------------------------------------------ linear (decode)
 
-__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -131,29 +125,51 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
   return v;
 }
 
-// Dequantise one word (8 codes) into the 4 A-fragment registers, times the
-// row scales (s_lo for rows g, s_hi for rows g+8, both bf16x2 {s, s}).  The mask
-// keeps bits 6-8 and 15 of each half (mantissa MSB, the two low exponent bits,
-// sign): a code lands as the bf16 fp4 * 2^-126.  Registers 1 and 2 are rotations;
-// register 3 multiplies the masked word by 2^2 + 2^7 + 2^12, three copies that
-// share no bit, so the sum never carries.  8 integer operations per word.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s_lo, uint32_t s_hi, uint32_t (&a)[4]) {
+// Multipliers of the register dequant, kept in constant memory so that the compiler
+// issues them as integer multiplies (FMA pipe) rather than as shift-add sequences
+// and LEAs, which share the ALU pipe with the masks, rotations and byte permutes.
+__constant__ uint32_t c_deq_mul[2] = {0x1084u, 16u};
+
+// a * {s.lo, s.lo} and a * {s.hi, s.hi} (bf16x2, round to nearest even)
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("{.reg .b16 l, h; .reg .b32 t; mov.b32 {l, h}, %2; mov.b32 t, {l, l}; mul.rn.bf16x2 %0, %1, t;}"
+      : "=r"(d) : "r"(a), "r"(s));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("{.reg .b16 l, h; .reg .b32 t; mov.b32 {l, h}, %2; mov.b32 t, {h, h}; mul.rn.bf16x2 %0, %1, t;}"
+      : "=r"(d) : "r"(a), "r"(s));
+  return d;
+}
+
+// Dequantise one word (8 codes) into the 4 A-fragment registers, times the row
+// scales s2 = bf16x2 {S(row g), S(row g+8)}.  The mask keeps bits 6-8 and 15 of each
+// half (mantissa MSB, the two low exponent bits, sign): a code lands as the bf16
+// fp4 * 2^-126.  Registers 1 and 2 are rotations of w by 10 and 13; register 3
+// multiplies the masked word by 2^2 + 2^7 + 2^12, three copies that share no bit, so
+// the sum never carries.  8 integer operations per word.  (Rotations as widening
+// multiplies measured slower: 17.6 against 15.8 us for a 17408 x 5120 decode.)
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t (&a)[4]) {
   constexpr uint32_t kMask = 0x81C081C0u;
   const uint32_t r0 = w & kMask;
   const uint32_t r1 = __funnelshift_l(w, w, 10) & kMask;
   const uint32_t r2 = __funnelshift_l(w, w, 13) & kMask;
-  const uint32_t r3 = ((w & 0x001B001Bu) * 0x1084u) & kMask;
-  a[0] = hmul2_bf16(r0, s_lo);
-  a[1] = hmul2_bf16(r1, s_hi);
-  a[2] = hmul2_bf16(r2, s_lo);
-  a[3] = hmul2_bf16(r3, s_hi);
+  const uint32_t r3 = ((w & 0x001B001Bu) * c_deq_mul[0]) & kMask;
+  a[0] = hmul2_lo(r0, s2);
+  a[1] = hmul2_hi(r1, s2);
+  a[2] = hmul2_lo(r2, s2);
+  a[3] = hmul2_hi(r3, s2);
 }
 
-// bf16x2 {S, S} with S = 0x7000 | b << 4 for the scale byte b at byte index `idx` of
-// `word`: one byte permute ({b, 0, b, 0}) and one multiply-add.
-__device__ __forceinline__ uint32_t scale_pair(uint32_t word, int idx) {
-  const uint32_t v = __byte_perm(word, 0u, static_cast<uint32_t>(idx) * 0x0101u + 0x4040u);
-  return v * 16u + 0x70007000u;
+// The scale pair of word j of a block: bf16x2 {S(g), S(g+8)} with S = 0x7000 | b << 4
+// for the bytes b of rows g and g+8 at bytes 2 (j & 1) and 2 (j & 1) + 1 of `word`
+// (the scale word of j < 2 or of j >= 2): one byte permute ({b_g, 0, b_g8, 0}) and
+// one multiply-add.
+__device__ __forceinline__ uint32_t scale_pair(uint32_t word, int j) {
+  const uint32_t v = __byte_perm(word, 0u, static_cast<uint32_t>(j & 1) * 0x0202u + 0x4140u);
+  return v * c_deq_mul[1] + 0x70007000u;
 }
 
 constexpr int kDecodeNT = 8;                    // 16-row n-tiles per CTA (128 rows)
@@ -312,10 +328,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
           for (int j2 = 0; j2 < 2; ++j2) {
             const int j = 2 * jj + j2;
             const uint32_t sword = j < 2 ? sc.x : sc.y;
-            const uint32_t s_lo = scale_pair(sword, (j & 1) * 2);
-            const uint32_t s_hi = scale_pair(sword, (j & 1) * 2 + 1);
             uint32_t a[4];
-            dequant_word(words[j], s_lo, s_hi, a);
+            dequant_word(words[j], scale_pair(sword, j), a);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[j2][mt], a, b[mt][2 * j2], b[mt][2 * j2 + 1]);
           }
@@ -428,6 +442,435 @@ nvfp4_status launch_decode(const CUtensorMap& tmW, const CUtensorMap& tmX, float
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, alpha_col, y, M, N, K, S));
+}
+
+// ------------------------------------------------------------------ linear, stream-K decode
+//
+// The balanced form of the decode kernel (TileLang PR #3290, Design: the persistent
+// stream-K kernel walking contiguous ranges of the (tile, k-tile) space, with a
+// deterministic fix-up of split tiles).  The work is the sequence of units (group of
+// 256 weight rows, 64-K block) in group-major order, and block i of G takes units
+// [i U / G, (i + 1) U / G) -- equal shares to within one unit, whatever N and K.
+//   warp 16     TMA producer: per stage one group's next <= 4 blocks (16 n-tiles x
+//               4 blocks, 36 KB) and the matching x columns, into a ring
+//   warps 0-15  n-tile w of every stage: register dequant + mma.sync (as the
+//               cluster kernel), accumulating over the block's units of a group.
+// A group wholly inside a block's range is written to y at once.  A block's first
+// and last groups may be split with its neighbours: for those it stores its FP32
+// partial in the caller's workspace as soon as the group's part ends, and at the end
+// of its range takes one ticket per split group.  The block that takes a group's last
+// ticket adds every part's partial in part order (so the result does not depend on
+// which part finishes last), writes y and zeroes the ticket.  No block waits for
+// another, and no warp stops in the middle of its range: a group's middle parts end
+// with their blocks' ranges anyway, so the tickets lose nothing by waiting for it.
+namespace skd {
+
+constexpr int kNT = 16;                                  // n-tiles per group (256 rows)
+constexpr int kWarps = 16;                               // consumer warps, one n-tile each
+constexpr int kThreads = 32 * (kWarps + 1);              // + the producer warp
+constexpr int kStageBlocks = 4;                          // 64-K blocks per full stage
+constexpr int kWBytes = kNT * kStageBlocks * kBlockBytes;  // 36 KB
+constexpr int kMaxTokens = 32;
+constexpr int kSlotFloats = kMaxTokens * kNT * 16;       // workspace per slot and SM: [32 tokens][256 rows]
+constexpr int kSmemLimit = 232448;                       // opt-in maximum per block
+constexpr int kMaxParts = 512;                           // blocks per grid (<= 2 per SM)
+
+// Up to 16 tokens two blocks share an SM (32 consumer warps per SM; the register
+// budget allows it), each with a 2-stage ring; 32 tokens run one block per SM with
+// as many stages (up to 5) as shared memory holds.
+__host__ __device__ constexpr int per_sm(int Mpad) { return Mpad <= 16 ? 2 : 1; }
+__host__ __device__ constexpr int stage_bytes(int Mpad) { return kWBytes + Mpad * kStageBlocks * 128; }
+__host__ __device__ constexpr int ring(int Mpad) {
+  return per_sm(Mpad) == 2 ? 2
+         : (kSmemLimit - 4096) / stage_bytes(Mpad) < 5 ? (kSmemLimit - 4096) / stage_bytes(Mpad) : 5;
+}
+__host__ __device__ constexpr int bar_off(int Mpad) { return ring(Mpad) * stage_bytes(Mpad); }
+// barriers (2 x 5 x 8 bytes), the abort flag and two last-ticket flags, the part list
+// of a split group, alignment slack
+__host__ __device__ constexpr int smem_bytes(int Mpad) { return bar_off(Mpad) + 96 + 4 * kMaxParts + 1024; }
+
+// First unit of block i of G over U units (U < 2^31, checked by the host).
+__host__ __device__ __forceinline__ int unit_start(int i, int G, int U) {
+  return static_cast<int>(static_cast<int64_t>(i) * U / G);
+}
+// The block whose range holds unit u.
+__device__ __forceinline__ int cta_of(int u, int G, int U) {
+  int i = static_cast<int>((static_cast<int64_t>(u) * G) / U);
+  while (i + 1 < G && unit_start(i + 1, G, U) <= u) ++i;
+  while (i > 0 && unit_start(i, G, U) > u) --i;
+  return i;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, per_sm(8 * MT))
+    w4a16_decode_sk_kernel(const __grid_constant__ CUtensorMap tmW4, const __grid_constant__ CUtensorMap tmW1,
+                           const __grid_constant__ CUtensorMap tmX, float alpha128, const float* __restrict__ alpha_col,
+                           __nv_bfloat16* __restrict__ y, int M, int N, int K, float* __restrict__ partials,
+                           int* __restrict__ tickets) {
+  constexpr int Mpad = 8 * MT;
+  constexpr int kStage = stage_bytes(Mpad);
+  constexpr int R = ring(Mpad);
+  constexpr int kXBytes = Mpad * kStageBlocks * 128;
+  constexpr int kSlot = Mpad * 256;  // floats per partial slot: [Mpad tokens][256 rows]
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t bar_full = sbase + bar_off(Mpad);
+  const uint32_t bar_empty = bar_full + 8 * 5;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + bar_off(Mpad) + 80);
+  volatile int* last_flag = abort_flag + 1;  // [2]: first and last group of the range
+  int* part_slot = reinterpret_cast<int*>(smem + bar_off(Mpad) + 96);  // [kMaxParts]
+
+  const int G = gridDim.x;
+  const int KB = K / 64;
+  const int NG = (N + 255) / 256;
+  const int U = NG * KB;
+  const int u0 = unit_start(blockIdx.x, G, U), u1 = unit_start(blockIdx.x + 1, G, U);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < R; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_launch_dependents();
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmW4);
+      prefetch_tensormap(&tmW1);
+      prefetch_tensormap(&tmX);
+      auto load_w = [&](int s, int u, int nblk) {
+        const int st = s % R;
+        const int g = u / KB, kb = u - g * KB;
+        const uint32_t dst = sbase + st * kStage;
+        mbar_arrive_expect_tx(bar_full + 8 * st, nblk * kNT * kBlockBytes + kXBytes);
+        if (nblk == kStageBlocks) {
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+              "l"(&tmW4), "r"(0), "r"(kb), "r"(g * kNT), "r"(bar_full + 8 * st)
+              : "memory");
+        } else {
+          // a segment's last 1-3 blocks: one box per block, [block][n-tile][576 B]
+          for (int j = 0; j < nblk; ++j)
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst + j * kNT * kBlockBytes),
+                "l"(&tmW1), "r"(0), "r"(kb + j), "r"(g * kNT), "r"(bar_full + 8 * st)
+                : "memory");
+        }
+      };
+      auto load_x = [&](int s, int u) {
+        const int st = s % R;
+        const int kb = u % KB;
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + st * kStage + kWBytes),
+            "l"(&tmX), "r"(0), "r"(0), "r"(kb), "r"(bar_full + 8 * st)
+            : "memory");
+      };
+      auto stage_len = [&](int u) {
+        const int seg_end = min(u1, (u / KB + 1) * KB);
+        return min(kStageBlocks, seg_end - u);
+      };
+      // The weights never depend on an earlier kernel: the first R stages' weights are
+      // requested before waiting for the previous grid in the stream (which may be
+      // producing x); their x columns follow the wait.
+      int s = 0;
+      int u = u0;
+      for (; s < R && u < u1; ++s) {
+        const int n = stage_len(u);
+        load_w(s, u, n);
+        u += n;
+      }
+      griddep_wait();
+      {
+        int v = u0;
+        for (int i = 0; i < s; ++i) {
+          load_x(i, v);
+          v += stage_len(v);
+        }
+      }
+      for (; u < u1; ++s) {
+        const int st = s % R;
+        if (!mbar_wait(bar_empty + 8 * st, ((s / R) - 1) & 1, abort_flag)) break;
+        const int n = stage_len(u);
+        load_w(s, u, n);
+        load_x(s, u);
+        u += n;
+      }
+      // Let every issued copy land before the thread block can exit.
+      for (int i = s > R ? s - R : 0; i < s; ++i)
+        mbar_wait_for(bar_full + 8 * (i % R), (i / R) & 1, 2000000000ull);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  griddep_wait();  // x, y and the workspace may belong to the previous grid in the stream
+  const int nt = warp;
+  const int gq = lane >> 2, t = lane & 3;
+  const uint32_t row_off = static_cast<uint32_t>(lane & 7) * 128u;
+  const uint32_t sw = static_cast<uint32_t>(lane & 7);
+  const uint32_t q = static_cast<uint32_t>(lane >> 3);
+
+  float acc[2][MT][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) acc[a][mt][0] = acc[a][mt][1] = acc[a][mt][2] = acc[a][mt][3] = 0.f;
+
+  auto do_block = [&](uint32_t blk, uint32_t xblk) {
+    uint4 c;
+    uint2 sc;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
+                 : "r"(blk + 16 * lane));
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sc.x), "=r"(sc.y) : "r"(blk + 512 + 8 * gq));
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      uint32_t bf[MT][4];
+      const uint32_t piece = ((4u * jj + q) ^ sw) * 16u;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) ldsm_x4(xblk + mt * 1024 + piece, bf[mt][0], bf[mt][1], bf[mt][2], bf[mt][3]);
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        const int j = 2 * jj + j2;
+        const uint32_t sword = j < 2 ? sc.x : sc.y;
+        uint32_t a[4];
+        dequant_word(words[j], scale_pair(sword, j), a);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[j2][mt], a, bf[mt][2 * j2], bf[mt][2 * j2 + 1]);
+      }
+    }
+  };
+
+  // y = bf16(sum * scale) for 4 rows of one token, rows row..row+3 of the output.
+  auto store4 = [&](float4 sum, int tok, int row) {
+    float4 scl = make_float4(alpha128, alpha128, alpha128, alpha128);
+    if (alpha_col != nullptr) {
+      const float4 a = *reinterpret_cast<const float4*>(alpha_col + row);
+      scl = make_float4(a.x * 128.0f, a.y * 128.0f, a.z * 128.0f, a.w * 128.0f);
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(sum.x * scl.x, sum.y * scl.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(sum.z * scl.z, sum.w * scl.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(y + static_cast<size_t>(tok) * N + row) = packed;
+  };
+
+  // After a timed-out wait (ok false) a warp still walks every stage and segment end
+  // without touching the data, so that the named barriers and the tickets stay
+  // consistent across the block's warps and across blocks.
+  int s = 0;
+  bool ok = true;
+  int seg_start = u0;
+  int g = u0 / KB;  // the group of the current segment, advanced without dividing
+  int gbeg = g * KB, gend = gbeg + KB;
+  int seg_end = min(u1, gend);
+  int split_group[2] = {-1, -1};  // split groups whose partial is in slot 2i (first) / 2i + 1 (last)
+  for (int u = u0; u < u1;) {
+    const int nblk = min(kStageBlocks, seg_end - u);
+    const int st = s % R;
+    if (ok) ok = warp_wait(bar_full + 8 * st, (s / R) & 1, abort_flag);
+    const uint32_t stage = sbase + st * kStage;
+    const uint32_t xstage = stage + kWBytes + row_off;
+    if (ok) {
+      if (nblk == kStageBlocks) {
+        // [n-tile][block][576 B]
+        const uint32_t tile = stage + nt * (kStageBlocks * kBlockBytes);
+#pragma unroll
+        for (int b = 0; b < kStageBlocks; ++b) do_block(tile + b * kBlockBytes, xstage + b * Mpad * 128);
+      } else {
+        // a segment's last 1-3 blocks: [block][n-tile][576 B]
+        const uint32_t tile = stage + nt * kBlockBytes;
+#pragma unroll 1
+        for (int b = 0; b < nblk; ++b) do_block(tile + b * (kNT * kBlockBytes), xstage + b * Mpad * 128);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+    ++s;
+    u += nblk;
+    if (u != seg_end) continue;
+
+    // ---------------------------------------------------------- end of a group segment
+    const int row_lo = g * 256 + nt * 16 + gq;  // and row_lo + 8
+    float v[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[mt][e] = acc[0][mt][e] + acc[1][mt][e];
+        acc[0][mt][e] = acc[1][mt][e] = 0.f;
+      }
+    if (seg_start == gbeg && seg_end == gend) {
+      // the whole group in this block
+      if (row_lo < N) {
+        const float s_lo = alpha_col != nullptr ? alpha_col[row_lo] * 128.0f : alpha128;
+        const float s_hi = alpha_col != nullptr ? alpha_col[row_lo + 8] * 128.0f : alpha128;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int tok = 8 * mt + 2 * t;
+          if (tok < M) {
+            y[static_cast<size_t>(tok) * N + row_lo] = __float2bfloat16_rn(v[mt][0] * s_lo);
+            y[static_cast<size_t>(tok) * N + row_lo + 8] = __float2bfloat16_rn(v[mt][2] * s_hi);
+          }
+          if (tok + 1 < M) {
+            y[static_cast<size_t>(tok + 1) * N + row_lo] = __float2bfloat16_rn(v[mt][1] * s_lo);
+            y[static_cast<size_t>(tok + 1) * N + row_lo + 8] = __float2bfloat16_rn(v[mt][3] * s_hi);
+          }
+        }
+      }
+    } else {
+      // a part of a split group: its partial goes to the workspace now, its ticket
+      // at the end of the range
+      const int which = seg_start == u0 ? 0 : 1;
+      split_group[which] = g;
+      float* dst = partials + static_cast<size_t>(2 * blockIdx.x + which) * kSlot;
+      const int r = nt * 16 + gq;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int tok = 8 * mt + 2 * t;
+        if (tok < M) {
+          dst[tok * 256 + r] = v[mt][0];
+          dst[tok * 256 + r + 8] = v[mt][2];
+        }
+        if (tok + 1 < M) {
+          dst[(tok + 1) * 256 + r] = v[mt][1];
+          dst[(tok + 1) * 256 + r + 8] = v[mt][3];
+        }
+      }
+    }
+    seg_start = seg_end;
+    ++g;
+    gbeg = gend;
+    gend += KB;
+    seg_end = min(u1, gend);
+  }
+
+  // ------------------------------------------------------------ tickets of split groups
+  if (split_group[0] < 0 && split_group[1] < 0) return;
+  named_bar_sync(1, 32 * kWarps);  // every consumer's partial stores are issued
+  if (lane == 0 && warp < 2 && split_group[warp] >= 0) {
+    // warp 0 takes the first group's ticket, warp 1 the last group's.  The barrier
+    // orders the other threads' partial stores before this release; its acquire
+    // half orders the partial loads below (after the next barrier) after it.
+    const int gg = split_group[warp];
+    const int first = cta_of(gg * KB, G, U), last = cta_of(gg * KB + KB - 1, G, U);
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(tickets + first) : "memory");
+    const int is_last = old == last - first;
+    if (is_last) tickets[first] = 0;
+    last_flag[warp] = is_last;
+  }
+  named_bar_sync(1, 32 * kWarps);
+  // The ring is free now (every stage was consumed): it holds the chunk sums below.
+  float4* chunk = reinterpret_cast<float4*>(smem);
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    const int gg = split_group[which];
+    if (gg < 0 || last_flag[which] == 0) continue;
+    // This block took the group's last ticket: add the parts in part order.  With few
+    // outputs (64 x M float4 of 4 rows) each output's parts are split into tpo
+    // contiguous chunks, one per thread, and the chunk sums added in chunk order.
+    const int first = cta_of(gg * KB, G, U), last = cta_of(gg * KB + KB - 1, G, U);
+    const int P = last - first + 1;
+    for (int p = threadIdx.x; p < P; p += 32 * kWarps)
+      part_slot[p] = 2 * (first + p) + (unit_start(first + p, G, U) >= gg * KB ? 0 : 1);
+    named_bar_sync(1, 32 * kWarps);
+    const int O = 64 * M;
+    const int tpo = O >= 32 * kWarps ? 1 : (32 * kWarps) / O;  // 1, 2, 4 or 8 (M = 1 .. 8)
+    for (int idx = threadIdx.x; idx < O * tpo; idx += 32 * kWarps) {
+      const int o = idx / tpo, j = idx - o * tpo;
+      const int tok = o >> 6, r4 = 4 * (o & 63);
+      const int p0 = j * P / tpo, p1 = (j + 1) * P / tpo;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int p = p0; p < p1; ++p) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(
+            partials + static_cast<size_t>(part_slot[p]) * kSlot + tok * 256 + r4));
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+      }
+      if (tpo == 1) {
+        if (gg * 256 + r4 < N) store4(sum, tok, gg * 256 + r4);
+      } else {
+        chunk[idx] = sum;
+      }
+    }
+    named_bar_sync(1, 32 * kWarps);
+    if (tpo > 1) {
+      for (int o = threadIdx.x; o < O; o += 32 * kWarps) {
+        const int tok = o >> 6, r4 = 4 * (o & 63);
+        float4 sum = chunk[o * tpo];
+        for (int j = 1; j < tpo; ++j) {
+          const float4 v = chunk[o * tpo + j];
+          sum.x += v.x;
+          sum.y += v.y;
+          sum.z += v.z;
+          sum.w += v.w;
+        }
+        if (gg * 256 + r4 < N) store4(sum, tok, gg * 256 + r4);
+      }
+      named_bar_sync(1, 32 * kWarps);  // chunk and part_slot are reused for the other group
+    }
+  }
+}
+
+}  // namespace skd
+
+// Two partial slots per block: [Mpad tokens][256 rows] floats, at most 2 x SMs blocks
+// of up to 16 tokens or SMs blocks of 32; then one ticket per block.
+size_t w4a16_streamk_workspace_bytes_for(int num_sms) {
+  return static_cast<size_t>(2) * num_sms * skd::kSlotFloats * sizeof(float) + static_cast<size_t>(num_sms) * 8 + 256;
+}
+
+template <int MT>
+nvfp4_status launch_decode_sk(const CUtensorMap& tmW4, const CUtensorMap& tmW1, const CUtensorMap& tmX,
+                              float alpha128, const float* alpha_col, __nv_bfloat16* y, int M, int N, int K,
+                              void* ws, cudaStream_t stream, const DeviceInfo& dev) {
+  auto kern = skd::w4a16_decode_sk_kernel<MT>;
+  const int smem = skd::smem_bytes(8 * MT);
+  if (static_cast<size_t>(smem) > dev.max_smem_optin) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+  static PerDeviceOnce smem_attr;
+  if (!smem_attr.get(dev.device, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+      }))
+    return NVFP4_ERR_CUDA;
+  // At most one block per unit, so that every block's range is non-empty: the parts
+  // of a split group are then exactly the blocks from the one holding its first unit
+  // to the one holding its last, and each of them takes one ticket.
+  const int64_t U = static_cast<int64_t>((N + 255) / 256) * (K / 64);
+  if (U > (int64_t(1) << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  const int slots = dev.num_sms * skd::per_sm(8 * MT);
+  const int G = static_cast<int>(U < slots ? U : slots);
+  if (G > skd::kMaxParts) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+  float* partials = static_cast<float*>(ws);
+  int* tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) +
+                                        static_cast<size_t>(2) * dev.num_sms * skd::kSlotFloats * sizeof(float));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G, 1, 1);
+  cfg.blockDim = dim3(skd::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as in launch_decode
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return from_cuda(
+      cudaLaunchKernelEx(&cfg, kern, tmW4, tmW1, tmX, alpha128, alpha_col, y, M, N, K, partials, tickets));
 }
 
 // ------------------------------------------------------------------ linear (tensor cores)
@@ -659,7 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 4; ++j) {
         const uint32_t sword = j < 2 ? sc.x : sc.y;
         uint32_t a[4];
-        dequant_word(words[j], scale_pair(sword, (j & 1) * 2), scale_pair(sword, (j & 1) * 2 + 1), a);
+        dequant_word(words[j], scale_pair(sword, j), a);
         const uint32_t p0 = static_cast<uint32_t>(((2 * j) ^ g) * 16);
         const uint32_t p1 = static_cast<uint32_t>(((2 * j + 1) ^ g) * 16);
         asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_lo + p0), "r"(a[0]) : "memory");
@@ -901,6 +1344,29 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
     if (st != NVFP4_OK) return st;
   }
   return NVFP4_OK;
+}
+
+size_t w4a16_streamk_workspace_bytes(const DeviceInfo& dev) { return w4a16_streamk_workspace_bytes_for(dev.num_sms); }
+
+nvfp4_status launch_w4a16_linear_streamk(const void* x, const void* Wprep, float alpha, const float* alpha_col,
+                                         void* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t stream,
+                                         const DeviceInfo& dev) {
+  // More than 32 tokens: the tensor-core kernel, which needs no workspace.
+  if (M > skd::kMaxTokens) return launch_w4a16_linear(x, Wprep, alpha, alpha_col, y, M, N, K, stream, dev);
+  const float alpha128 = alpha * 128.0f;
+  CUtensorMap tmW4, tmW1, tmX;
+  nvfp4_status st = encode_tmap_wprep(&tmW4, Wprep, N, K, skd::kStageBlocks, skd::kNT);
+  if (st == NVFP4_OK) st = encode_tmap_wprep(&tmW1, Wprep, N, K, 1, skd::kNT);
+  const int MT = M <= 8 ? 1 : M <= 16 ? 2 : 4;
+  if (st == NVFP4_OK) st = encode_tmap_x_blocks(&tmX, x, M, K, 8 * MT, skd::kStageBlocks);
+  if (st != NVFP4_OK) return st;
+  auto* yb = static_cast<__nv_bfloat16*>(y);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  switch (MT) {
+    case 1: return launch_decode_sk<1>(tmW4, tmW1, tmX, alpha128, alpha_col, yb, m, n, k, ws, stream, dev);
+    case 2: return launch_decode_sk<2>(tmW4, tmW1, tmX, alpha128, alpha_col, yb, m, n, k, ws, stream, dev);
+    default: return launch_decode_sk<4>(tmW4, tmW1, tmX, alpha128, alpha_col, yb, m, n, k, ws, stream, dev);
+  }
 }
 
 }  // namespace nvfp4
