@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the sub-measurements")
-    ap.add_argument("--only", choices=["w4a16", "producers", "llm"], default=None,
+    ap.add_argument("--only", choices=["w4a16", "producers", "llm", "mma_ceiling"], default=None,
                     help="run one sub-measurement alone and print its JSON (for profiling runs)")
     ap.add_argument("--w4a16-shapes", default=None,
                     help="with --only w4a16: comma-separated NxKxM list, e.g. 17408x5120x1")
@@ -588,6 +588,23 @@ def bench_producers(peaks):
     return res
 
 
+def bench_mma_ceiling(iters=8192):
+    """Back-to-back tcgen05 CTA-pair MMAs (M = N = 256, operands resident) per kind:
+    the instruction ceiling the GEMM can reach, and the hardware's FP4 : BF16 ratio."""
+    import nvfp4_block_scaled_gb300 as nv
+
+    out = {}
+    for kind in ("bf16", "fp8", "nvf4"):
+        best = None
+        for _ in range(3):
+            tf, cyc = nv.mma_ceiling(kind, iters)
+            if best is None or tf > best[0]:
+                best = (tf, cyc)
+        out[kind] = {"tflops": round(best[0], 1), "cycles_per_mma": round(best[1], 1)}
+    out["nvf4_over_bf16"] = round(out["nvf4"]["tflops"] / out["bf16"]["tflops"], 3)
+    return out
+
+
 def cpu_baseline_gemm(S, target_s=12.0, max_samples=1 << 16):
     """The oracle on a bounded sample of the S^3 workload: sampled outputs, each a full
     K-length dot product of dequantised rows (float64).  Returns TFLOP/s."""
@@ -661,6 +678,12 @@ def run_ours(args):
     }
     if rank == 0:
         line["clocks"] = sampler.summary() if sampler else None
+        # the FP4 instruction ceiling measured on this GPU, beside the nominal peak
+        ceil = bench_mma_ceiling()
+        line["roofline"]["mma_ceiling"] = {"nvf4_tflops": ceil["nvf4"]["tflops"],
+                                           "bf16_tflops": ceil["bf16"]["tflops"],
+                                           "nvf4_over_bf16": ceil["nvf4_over_bf16"],
+                                           "frac_of_nvf4_ceiling": round(achieved / ceil["nvf4"]["tflops"], 4)}
     if not args.quick:
         t16, _ = time_gemm(16384, 3, 2, world)
         line["gemm_16384"] = {"ms": round(statistics.mean(t16), 4),
@@ -754,6 +777,8 @@ def run_only(args):
         if args.llm_shapes:
             shapes = [tuple(int(v) for v in item.lower().split("x")) for item in args.llm_shapes.split(",")]
         out = bench_llm(peaks, tuple(int(c) for c in args.llm_configs.split(",")), shapes)
+    elif args.only == "mma_ceiling":
+        out = bench_mma_ceiling()
     else:
         out = bench_producers(peaks)
     print(json.dumps({"only": args.only, "results": out}), flush=True)

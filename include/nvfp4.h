@@ -400,6 +400,24 @@ nvfp4_status nvfp4_w4a16_linear_colscale(const void* x_bf16, const void* Wprep, 
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear);
 
 /*
+ * nvfp4_mma_ceiling -- diagnostic: the tensor-core instruction ceiling of the device.
+ *
+ * Every CTA pair issues `iters` tcgen05.mma.cta_group::2 instructions (M = 256, N = 256,
+ * operands resident in shared memory, FP32 accumulator in TMEM) of one kind back to
+ * back: kind 0 = block-scaled E2M1 (kind::mxf4nvf4, scale_vec::4X, the GEMM's
+ * instruction), 1 = BF16 (kind::f16), 2 = E4M3 (kind::f8f6f4).  Writes the achieved
+ * TFLOP/s over the slowest pair and the median clock cycles per instruction.  It is
+ * synchronous on `stream` and independent of any operand data.
+ *   kind     0, 1 or 2.
+ *   iters    instructions per pair, a multiple of 4 in [4, 2^24].
+ *   tflops, cycles_per_mma   HOST pointers (either may be NULL).
+ * Errors: NVFP4_ERR_INVALID_ARG for a bad kind or iters, NVFP4_ERR_TIMEOUT if the
+ * instructions did not complete within 2 s, NVFP4_ERR_CUDA, NVFP4_ERR_UNSUPPORTED_DEVICE.
+ */
+nvfp4_status nvfp4_mma_ceiling(int kind, int iters, double* tflops, double* cycles_per_mma,
+                               nvfp4_stream_t stream);
+
+/*
  * nvfp4_test_streamk_fault -- FOR TESTS ONLY: fault injection into the stream-K
  * schedule of nvfp4_gemm_streamk / nvfp4_gemm_streamk_noalloc on the current device.
  * No counterpart on the cited pages; it exists to exercise the timeout path without

@@ -11,7 +11,7 @@ Entry points (same names as the C ABI, without the ``nvfp4_`` prefix):
   gemm, gemm_streamk, gemm_streamk_workspace_bytes, gemm_streamk_noalloc,
   gemm_two_pass, gemm_config_name, gemm_choose_config, w4a16_prepared_bytes,
   w4a16_prepare, w4a16_linear, w4a16_linear_colscale, w4a16_streamk_workspace_bytes,
-  w4a16_linear_streamk, device_error.
+  w4a16_linear_streamk, mma_ceiling, device_error.
 
 Every entry point checks that each tensor it is given holds at least the bytes the
 call reads or writes (the C ABI takes raw pointers and cannot), and raises
@@ -33,7 +33,7 @@ ABI_SYMBOLS = (
     "nvfp4_gemm_streamk_workspace_bytes", "nvfp4_gemm_streamk_noalloc", "nvfp4_gemm_config_name",
     "nvfp4_gemm_choose_config", "nvfp4_w4a16_prepared_bytes", "nvfp4_w4a16_prepare",
     "nvfp4_w4a16_linear", "nvfp4_w4a16_linear_colscale", "nvfp4_w4a16_streamk_workspace_bytes",
-    "nvfp4_w4a16_linear_streamk", "nvfp4_device_error",
+    "nvfp4_w4a16_linear_streamk", "nvfp4_mma_ceiling", "nvfp4_device_error",
     "nvfp4_test_streamk_fault",
 )
 
@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "nvfp4_w4a16_linear": (c_i, [c_p, c_p, c_f, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_w4a16_linear_colscale": (c_i, [c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_p]),
         "nvfp4_w4a16_streamk_workspace_bytes": (ctypes.c_size_t, []),
+        "nvfp4_mma_ceiling": (c_i, [c_i, c_i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), c_p]),
         "nvfp4_w4a16_linear_streamk": (c_i, [c_p, c_p, c_f, c_p, c_p, c_i64, c_i64, c_i64, c_p, ctypes.c_size_t,
                                              c_p]),
         "nvfp4_device_error": (c_i, [c_p, c_i]),
@@ -417,6 +418,18 @@ def w4a16_linear_streamk(x, Wprep, alpha: float, N: int, workspace, alpha_col=No
         _ptr(x), _ptr(Wprep), float(alpha), _ptr(alpha_col) if alpha_col is not None else None, _ptr(out), M,
         int(N), K, _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+MMA_KINDS = {"nvf4": 0, "bf16": 1, "fp8": 2}
+
+
+def mma_ceiling(kind: str = "nvf4", iters: int = 8192, stream=None):
+    """nvfp4_mma_ceiling: (TFLOP/s, median cycles per instruction) of back-to-back
+    M = 256, N = 256 CTA-pair MMAs of `kind` ('nvf4', 'bf16' or 'fp8')."""
+    tf, cyc = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check("nvfp4_mma_ceiling", load_library().nvfp4_mma_ceiling(
+        MMA_KINDS[kind], int(iters), ctypes.byref(tf), ctypes.byref(cyc), _stream(stream)))
+    return tf.value, cyc.value
 
 
 def test_streamk_fault(skip_publish: bool, flag_wait_ns: int = 0) -> None:

@@ -373,6 +373,15 @@ nvfp4_status nvfp4_w4a16_linear_streamk(const void* x_bf16, const void* Wprep, f
                                      K, workspace, as_stream(stream), dev);
 }
 
+nvfp4_status nvfp4_mma_ceiling(int kind, int iters, double* tflops, double* cycles_per_mma,
+                               nvfp4_stream_t stream) {
+  if (kind < 0 || kind > 2 || iters < 4 || iters % 4 != 0 || iters > (1 << 24)) return NVFP4_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  nvfp4_status st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  return mma_ceiling(kind, iters, tflops, cycles_per_mma, as_stream(stream), dev);
+}
+
 nvfp4_status nvfp4_device_error(nvfp4_stream_t stream, int clear) {
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return NVFP4_ERR_CUDA;
   const int a = read_device_error_gemm(clear != 0);

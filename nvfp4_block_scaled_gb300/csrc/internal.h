@@ -125,4 +125,9 @@ nvfp4_status launch_w4a16_linear_streamk(const void* x, const void* Wprep, float
                                          void* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t stream,
                                          const DeviceInfo& dev);
 
+// Diagnostic: tcgen05 instruction ceiling for kind 0 (block-scaled FP4), 1 (BF16) or
+// 2 (E4M3); see nvfp4_mma_ceiling.
+nvfp4_status mma_ceiling(int kind, int iters, double* tflops, double* cycles_per_mma, cudaStream_t stream,
+                         const DeviceInfo& dev);
+
 }  // namespace nvfp4

@@ -98,6 +98,24 @@ def test_w4a16_argument_checks(lib):
     assert col(P, P, P, P, 1, 256, 320, None) == SHAPE
 
 
+def test_w4a16_streamk_argument_checks(lib):
+    f = ctypes.c_float(0.5)
+    sk = lib.nvfp4_w4a16_linear_streamk
+    assert sk(None, P, f, None, P, 1, 256, 512, P, 1 << 30, None) == INVALID
+    assert sk(P, P, f, None, P, 1, 192, 512, P, 1 << 30, None) == SHAPE   # N % 128
+    assert sk(P, P, f, None, P, 1, 256, 320, P, 1 << 30, None) == SHAPE   # K % 256
+    assert sk(P, P, ctypes.c_float(NAN), None, P, 1, 256, 512, P, 1 << 30, None) == INVALID
+    assert sk(P, P, f, P4, P, 1, 256, 512, P, 1 << 30, None) == MISALIGNED  # alpha_col
+    assert sk(P, P, f, None, P, 1, 256, 512, None, 1 << 30, None) == INVALID  # workspace
+    assert sk(P, P, f, None, P, 1, 256, 512, ODD, 1 << 30, None) == MISALIGNED
+
+
+def test_mma_ceiling_argument_checks(lib):
+    assert lib.nvfp4_mma_ceiling(3, 64, None, None, None) == INVALID
+    assert lib.nvfp4_mma_ceiling(0, 6, None, None, None) == INVALID
+    assert lib.nvfp4_mma_ceiling(0, 0, None, None, None) == INVALID
+
+
 def test_size_helpers_reject_invalid_shapes(lib):
     assert nv.packed_scales_bytes(0, 64) == 0 and nv.packed_scales_bytes(4, -16) == 0
     assert nv.w4a16_prepared_bytes(0, 256) == 0 and nv.w4a16_prepared_bytes(128, 100) == 0
