@@ -1,10 +1,12 @@
 // quantize.cu -- NVFP4 operand producers: BF16 -> E2M1 codes + E4M3 block scales,
 // and the row-major -> 128x4-atom scale-factor permutation.
 //
-// Both kernels are HBM-bound: quantize takes one 16-element block per thread
-// (coalesced 32-byte loads, 8-byte code stores) over a grid sized to a multiple of
-// the SM count, and can write its scales straight into the packed layout (fused
-// quantize + pack); pack_scales transposes 128-row bands through shared memory.
+// The kernels are HBM-bound.  Every quantiser takes one 16-element block per thread
+// (coalesced 32-byte loads, 8-byte code stores) over a grid-stride loop sized to a
+// multiple of the SM count; the fused and two-pass forms store each scale byte
+// straight at its place in the packed layout.  pack_scales is a permutation of
+// 32-bit words (each packed word is four consecutive scales of one row), done with
+// one load and one coalesced store per word.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -156,119 +158,91 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
   }
 }
 
-// Fused quantize + pack.  One thread block of 16 warps per (128-row band, 2 atoms
-// = 8 scale columns): lane l of a warp takes scale column 8*tile + l%8 of row
-// 4*(16*rr + w) + l/8 (rr = 0, 1), so a warp quantises four rows per step, reading
-// 256 contiguous bytes of each.  Two shuffles assemble each 4-scale word (one row's
-// scales of one atom) in the lane of its first column, which stores it at its place
-// in the packed layout (word 4*(r%32) + r/32 of the atom for row r of the band):
-// every word of the tile's atoms is written exactly once, padding rows and padding
-// columns as zero, with no shared-memory staging and no block barrier.  Small tiles
-// keep the last wave short (8192 x 5120 is 2560 tiles for about 304 resident blocks).
-// Rows past `rows` and scale columns past C give zero scale bytes and no codes.
-// (16 warps per block: the quantiser is bound by its arithmetic, so it wants the
-// SM's full 64 warps.)
-constexpr int kQPAtoms = 2;
-constexpr int kQPCols = 4 * kQPAtoms;        // scale columns per tile = lanes per row
-constexpr int kQPRowsPerWarp = 32 / kQPCols; // rows per warp and step
-constexpr int kQPThreads = 512;
-static_assert(32 % kQPCols == 0, "a warp covers whole rows of a tile");
+// ------------------------------------------------------------------ flat producers
+//
+// One 16-element block per thread over a grid-stride loop (the layout of
+// quantize_kernel: a warp reads 1 KB of contiguous x), each scale byte stored straight
+// at its place in the packed 128x4-atom layout.  The loop runs over the padded
+// [bands * 128 rows] x [4 * groups columns] scale grid, so padding positions (rows
+// past `rows`, columns past C) receive zero bytes and every byte of the packed buffer
+// is written exactly once.  Byte b of the packed buffer for (row r, scale column c):
+// ((r / 128 * groups + c / 4) * 128 + 4 * (r % 32) + (r % 128) / 32) * 4 + c % 4.
+template <typename I>
+__device__ __forceinline__ I packed_byte(I r, I c, I groups) {
+  return (((r >> 7) * groups + (c >> 2)) * 128 + 4 * (r & 31) + ((r >> 5) & 3)) * 4 + (c & 3);
+}
 
-__global__ void __launch_bounds__(kQPThreads) quantize_packed_kernel(const uint4* __restrict__ x, int64_t rows,
-                                                                     int64_t C, int64_t groups, int64_t tiles_per_band,
-                                                                     int64_t num_tiles, float g,
-                                                                     uint2* __restrict__ codes,
-                                                                     uint32_t* __restrict__ sf_packed) {
+// I: the index type (uint32_t when the padded grid, and so the packed buffer, has
+// fewer than 2^32 - 2^24 entries, so that no index passes 2^32 on the last stride).  The grid-stride loop advances (row, column) without a
+// division per step.
+template <typename I>
+__global__ void __launch_bounds__(256) quantize_packed_flat_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                   int64_t C, int64_t groups, int64_t total,
+                                                                   float g, uint2* __restrict__ codes,
+                                                                   uint8_t* __restrict__ sf_packed) {
   griddep_wait();  // x from the previous grid; dependents are signalled at completion (see quantize_kernel)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = lane % kQPCols, rsub = lane / kQPCols;
-  constexpr int kWarps = kQPThreads / 32;
-  for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const int64_t band = t / tiles_per_band;
-    const int64_t a0 = (t - band * tiles_per_band) * kQPAtoms;
-    const int64_t c = 4 * a0 + col;
-    const bool col_ok = c < C;
-    const bool atom_ok = a0 + (col >> 2) < groups;
-#pragma unroll
-    for (int rr = 0; rr < 128 / (kWarps * kQPRowsPerWarp); ++rr) {
-      const int row = (rr * kWarps + warp) * kQPRowsPerWarp + rsub;
-      const int64_t r = band * 128 + row;
-      uint32_t sbyte = 0;
-      if (col_ok && r < rows) {
-        const int64_t b = r * C + c;
-        uint32_t c0, c1;
-        sbyte = quantize_block(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), g, &c0, &c1);
-        __stcs(codes + b, make_uint2(c0, c1));
-      }
-      const uint32_t w1 = sbyte | (__shfl_down_sync(0xffffffffu, sbyte, 1) << 8);
-      const uint32_t w2 = w1 | (__shfl_down_sync(0xffffffffu, w1, 2) << 16);
-      if ((col & 3) == 0 && atom_ok)
-        sf_packed[(band * groups + a0 + (col >> 2)) * 128 + 4 * (row & 31) + (row >> 5)] = w2;
+  const I Cp = static_cast<I>(4 * groups), Ci = static_cast<I>(C), Rows = static_cast<I>(rows);
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  const I stride_r = stride / Cp, stride_c = stride - stride_r * Cp;
+  const I v0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x;
+  I r = v0 / Cp, c = v0 - r * Cp;
+  for (I v = v0; v < static_cast<I>(total); v += stride) {
+    uint32_t sbyte = 0;
+    if (r < Rows && c < Ci) {
+      const int64_t b = static_cast<int64_t>(r) * Ci + c;
+      uint32_t c0, c1;
+      sbyte = quantize_block(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), g, &c0, &c1);
+      __stcs(codes + b, make_uint2(c0, c1));
+    }
+    sf_packed[packed_byte<I>(r, c, static_cast<I>(groups))] = static_cast<uint8_t>(sbyte);
+    r += stride_r;
+    c += stride_c;
+    if (c >= Cp) {
+      c -= Cp;
+      ++r;
     }
   }
 }
 
-// Two-pass (value + residual) quantisation into the interleaved operand: per 256-
-// element K-block j of a row, the value codes (128 bytes) then the residual codes
-// (128 bytes), so a row holds 2K codes; the scales in the packed layout of a
-// [rows x 2K] operand, where K-block j's value scales fill atoms 8j..8j+3 and its
-// residual scales atoms 8j+4..8j+7.  One thread block of 16 warps per (128-row band,
-// K-block j): lane l of a warp takes source block 16j + u (u = l mod 16) of row
-// 2*(16*rr + w) + l/16 (rr = 0..3) through both passes.  Its value codes land at
-// byte 256j + 8u of the row and its residual codes at 256j + 128 + 8u (two 128-byte
-// runs per row and pass), and its two scales are assembled into atom words by
-// shuffles as in quantize_packed_kernel: value word u/4 and residual word 4 + u/4
-// of the tile's row.  One K-block per tile keeps the last wave short (8192 x 5120 is
-// 1280 tiles for 304 resident blocks).  Rows past `rows` give zero scales and no codes.
-constexpr int kTPPitch = 8 + 1;  // atom words per tile row (one K-block), padded
-
-__global__ void __launch_bounds__(kQPThreads) quantize_two_pass_kernel(const uint4* __restrict__ x, int64_t rows,
-                                                                       int64_t C, int64_t kblocks, int64_t num_tiles,
-                                                                       float g, uint2* __restrict__ codes,
-                                                                       uint32_t* __restrict__ sf_packed) {
-  __shared__ uint32_t tile[128 * kTPPitch];
+// Two-pass quantisation, one source block per thread: block (r, c = 16 j + u) of x
+// gives value codes at code block 32 j + u of row r's 2K codes and residual codes at
+// 32 j + 16 + u, and its two scales at those columns of the packed [rows x 2K]
+// operand (K % 256 == 0, so the scale columns need no padding; rows are padded to 128).
+template <typename I>
+__global__ void __launch_bounds__(256) quantize_two_pass_flat_kernel(const uint4* __restrict__ x, int64_t rows,
+                                                                     int64_t C, int64_t total, float g,
+                                                                     uint2* __restrict__ codes,
+                                                                     uint8_t* __restrict__ sf_packed) {
   griddep_wait();  // x from the previous grid; dependents are signalled at completion (see quantize_kernel)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u = lane & 15, rsub = lane >> 4;
-  constexpr int kWarps = kQPThreads / 32;
-  const int64_t groups = 8 * kblocks;  // scale atoms per band of the [rows x 2K] operand
-  for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const int64_t band = t / kblocks;
-    const int64_t j = t - band * kblocks;
-#pragma unroll 1
-    for (int rr = 0; rr < 128 / (2 * kWarps); ++rr) {
-      const int row = (rr * kWarps + warp) * 2 + rsub;
-      const int64_t r = band * 128 + row;
-      uint32_t s1 = 0, s2 = 0;
-      if (r < rows) {
-        const int64_t b = r * C + 16 * j + u;
-        float f[16];
-        unpack_bf16x16(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), f);
-        uint32_t c0, c1, d0, d1;
-        s1 = quantize_floats(f, g, &c0, &c1);
-        float rf[16];
-        residual_block(f, c0, c1, s1, g, rf);
-        s2 = quantize_floats(rf, g, &d0, &d1);
-        uint2* crow = codes + r * 2 * C + 32 * j;
-        __stcs(crow + u, make_uint2(c0, c1));
-        __stcs(crow + 16 + u, make_uint2(d0, d1));
-      }
-      const uint32_t a1 = s1 | (__shfl_down_sync(0xffffffffu, s1, 1) << 8);
-      const uint32_t w1 = a1 | (__shfl_down_sync(0xffffffffu, a1, 2) << 16);
-      const uint32_t a2 = s2 | (__shfl_down_sync(0xffffffffu, s2, 1) << 8);
-      const uint32_t w2 = a2 | (__shfl_down_sync(0xffffffffu, a2, 2) << 16);
-      if ((u & 3) == 0) {
-        tile[row * kTPPitch + (u >> 2)] = w1;
-        tile[row * kTPPitch + 4 + (u >> 2)] = w2;
-      }
+  const I Ci = static_cast<I>(C), Rows = static_cast<I>(rows), groups2 = static_cast<I>((2 * C) / 4);
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  const I stride_r = stride / Ci, stride_c = stride - stride_r * Ci;
+  const I v0 = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x;
+  I r = v0 / Ci, c = v0 - r * Ci;
+  for (I v = v0; v < static_cast<I>(total); v += stride) {
+    const I cv = 2 * c - (c & 15);  // 32 j + u
+    uint32_t s1 = 0, s2 = 0;
+    if (r < Rows) {
+      const int64_t b = static_cast<int64_t>(r) * Ci + c;
+      float f[16];
+      unpack_bf16x16(__ldcs(x + 2 * b), __ldcs(x + 2 * b + 1), f);
+      uint32_t c0, c1, d0, d1;
+      s1 = quantize_floats(f, g, &c0, &c1);
+      float rf[16];
+      residual_block(f, c0, c1, s1, g, rf);
+      s2 = quantize_floats(rf, g, &d0, &d1);
+      uint2* crow = codes + static_cast<int64_t>(r) * 2 * C;
+      __stcs(crow + cv, make_uint2(c0, c1));
+      __stcs(crow + cv + 16, make_uint2(d0, d1));
     }
-    __syncthreads();
-    uint32_t* dst = sf_packed + (band * groups + 8 * j) * 128;
-    for (int i = threadIdx.x; i < 8 * 128; i += blockDim.x) {
-      const int a = i >> 7, wd = i & 127;
-      dst[i] = tile[(32 * (wd & 3) + (wd >> 2)) * kTPPitch + a];
+    sf_packed[packed_byte<I>(r, cv, groups2)] = static_cast<uint8_t>(s1);
+    sf_packed[packed_byte<I>(r, cv + 16, groups2)] = static_cast<uint8_t>(s2);
+    r += stride_r;
+    c += stride_c;
+    if (c >= Ci) {
+      c -= Ci;
+      ++r;
     }
-    __syncthreads();
   }
 }
 
@@ -371,26 +345,28 @@ nvfp4_status launch_quantize(const void* x, int64_t rows, int64_t K, float g, ui
                                         reinterpret_cast<uint2*>(codes), sf));
   }
   const int64_t groups = (C + 3) / 4;
-  const int64_t tiles_per_band = (groups + kQPAtoms - 1) / kQPAtoms;
-  const int64_t num_tiles = ((rows + 127) / 128) * tiles_per_band;
-  cudaLaunchConfig_t cfg = programmatic_config(grid_for(num_tiles * kQPThreads, kQPThreads, dev, 4), kQPThreads, stream);
+  const int64_t total = ((rows + 127) / 128) * 128 * (4 * groups);  // padded scale grid
+  cudaLaunchConfig_t cfg = programmatic_config(grid_for(total, 256, dev, 8), 256, stream);
   set_programmatic(cfg, attr);
-  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_packed_kernel, static_cast<const uint4*>(x), rows, C, groups,
-                                      tiles_per_band, num_tiles, g, reinterpret_cast<uint2*>(codes),
-                                      reinterpret_cast<uint32_t*>(sf)));
+  if (total < (int64_t(1) << 32) - (int64_t(1) << 24))
+    return from_cuda(cudaLaunchKernelEx(&cfg, quantize_packed_flat_kernel<uint32_t>, static_cast<const uint4*>(x),
+                                        rows, C, groups, total, g, reinterpret_cast<uint2*>(codes), sf));
+  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_packed_flat_kernel<int64_t>, static_cast<const uint4*>(x), rows,
+                                      C, groups, total, g, reinterpret_cast<uint2*>(codes), sf));
 }
 
 nvfp4_status launch_quantize_two_pass(const void* x, int64_t rows, int64_t K, float g, uint8_t* codes,
                                       uint8_t* sf_packed, cudaStream_t stream, const DeviceInfo& dev) {
   const int64_t C = K / 16;
-  const int64_t kblocks = K / 256;
-  const int64_t num_tiles = ((rows + 127) / 128) * kblocks;
+  const int64_t total = ((rows + 127) / 128) * 128 * C;  // rows padded to whole bands
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = programmatic_config(grid_for(num_tiles * kQPThreads, kQPThreads, dev, 4), kQPThreads, stream);
+  cudaLaunchConfig_t cfg = programmatic_config(grid_for(total, 256, dev, 8), 256, stream);
   set_programmatic(cfg, attr);
-  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_two_pass_kernel, static_cast<const uint4*>(x), rows, C, kblocks,
-                                      num_tiles, g, reinterpret_cast<uint2*>(codes),
-                                      reinterpret_cast<uint32_t*>(sf_packed)));
+  if (total < (int64_t(1) << 32) - (int64_t(1) << 24))
+    return from_cuda(cudaLaunchKernelEx(&cfg, quantize_two_pass_flat_kernel<uint32_t>, static_cast<const uint4*>(x),
+                                        rows, C, total, g, reinterpret_cast<uint2*>(codes), sf_packed));
+  return from_cuda(cudaLaunchKernelEx(&cfg, quantize_two_pass_flat_kernel<int64_t>, static_cast<const uint4*>(x),
+                                      rows, C, total, g, reinterpret_cast<uint2*>(codes), sf_packed));
 }
 
 nvfp4_status launch_pack_scales(const uint8_t* sf, int64_t rows, int64_t K, uint8_t* out, cudaStream_t stream,
