@@ -42,14 +42,6 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
   return r;
 }
 
-// Exact value of an E2M1 code nibble: bit 3 sign, bits 2..1 exponent (bias 1), bit 0
-// mantissa; 0 and 0.5 for exponent 0.
-__device__ __forceinline__ float e2m1_to_float(uint32_t n) {
-  const uint32_t e = (n >> 1) & 3u, m = n & 1u;
-  const float mag = e == 0 ? 0.5f * static_cast<float>(m) : __uint_as_float(((e + 126u) << 23) | (m << 22));
-  return (n & 8u) ? -mag : mag;
-}
-
 // The 16 floats of one block of bf16: v0, v1 = its 32 bytes.
 __device__ __forceinline__ void unpack_bf16x16(uint4 v0, uint4 v1, float (&f)[16]) {
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -131,14 +123,20 @@ __device__ __forceinline__ uint32_t quantize_block(uint4 v0, uint4 v1, float g, 
 
 // Residual of a quantised block: r_i = f_i - (value(code_i) * scale) * g, the product
 // exact (at most 5 significant bits), the multiply by g and the subtraction each one
-// IEEE float32 operation (no contraction).
+// IEEE float32 operation (no contraction).  value(code) * scale is formed without a
+// per-code branch: the code's magnitude bits placed at float bits 22..24 and its sign
+// at bit 31 give the float value(code) * 2^-126 (a subnormal for exponent field 0, as
+// E2M1's own subnormal), which two exact multiplies (by 2^100, then by scale * 2^26)
+// bring to value(code) * scale.
 __device__ __forceinline__ void residual_block(const float (&f)[16], uint32_t c0, uint32_t c1, uint32_t sbyte,
                                                float g, float (&r)[16]) {
-  const float sc = e4m3_to_float(sbyte);
+  const float sc26 = __fmul_rn(e4m3_to_float(sbyte), 67108864.0f);  // scale * 2^26, exact
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint32_t nib = ((i < 8 ? c0 : c1) >> (4 * (i & 7))) & 0xFu;
-    r[i] = __fsub_rn(f[i], __fmul_rn(__fmul_rn(e2m1_to_float(nib), sc), g));
+    const float v126 = __uint_as_float(((nib & 7u) << 22) | ((nib & 8u) << 28));  // value * 2^-126
+    const float vs = __fmul_rn(__fmul_rn(v126, 1.2676506002282294e30f), sc26);     // value * scale
+    r[i] = __fsub_rn(f[i], __fmul_rn(vs, g));
   }
 }
 
