@@ -307,8 +307,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
       const uint32_t stage = ring + st * kStage;
       const uint32_t tile = stage + nt * (kChunkKC * kBlockBytes);
       const uint32_t xstage = stage + kChunkBytes + row_off;
-#pragma unroll 1
-      for (int kc = kb0; kc < kb1; ++kc) {
+      auto do_block = [&](int kc) {
         const uint32_t blk = tile + kc * kBlockBytes;
         uint4 c;
         uint2 sc;
@@ -334,6 +333,14 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_min_blocks<MT>())
             for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[j2][mt], a, b[mt][2 * j2], b[mt][2 * j2 + 1]);
           }
         }
+      };
+      if (kb1 - kb0 == kChunkKC / 2) {
+        // a whole half chunk: unrolled (no loop branch, loads of the next block in flight)
+#pragma unroll
+        for (int u = 0; u < kChunkKC / 2; ++u) do_block(kb0 + u);
+      } else {
+#pragma unroll 1
+        for (int kc = kb0; kc < kb1; ++kc) do_block(kc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * st);
