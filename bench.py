@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="skip the sub-measurements")
-    ap.add_argument("--only", choices=["w4a16", "producers", "llm", "mma_ceiling"], default=None,
+    ap.add_argument("--only", choices=["w4a16", "producers", "llm", "mma_ceiling", "cublaslt"], default=None,
                     help="run one sub-measurement alone and print its JSON (for profiling runs)")
     ap.add_argument("--w4a16-shapes", default=None,
                     help="with --only w4a16: comma-separated NxKxM list, e.g. 17408x5120x1")
@@ -605,6 +605,61 @@ def bench_mma_ceiling(iters=8192):
     return out
 
 
+def bench_cublaslt(sizes=(S_MAIN,), steps=10):
+    """The vendor library's NVFP4 GEMM on the headline's own operands, beside ours: a
+    reference point, not part of the library's path.  cuBLASLt is reached through
+    torch._scaled_mm with FP4 operands and E4M3 scales per 16 elements in the same
+    128x4-atom layout that pack_scales writes; it has no alpha, so the bit-identity
+    check compares both at alpha = 1.  Both are timed like the headline (CUDA events
+    on the current stream, L2 flushed between iterations)."""
+    import torch
+
+    import nvfp4_block_scaled_gb300 as nv
+
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        return {"unavailable": f"PyTorch {torch.__version__} has no FP4 dtype"}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    out = {}
+    for S in sizes:
+        _, (a, sfa, b, sfb) = gemm_operands(S)
+        a4, b4 = a.view(torch.float4_e2m1fn_x2), b.view(torch.float4_e2m1fn_x2).t()
+        sa8, sb8 = sfa.view(torch.float8_e4m3fn), sfb.view(torch.float8_e4m3fn)
+        D = torch.empty((S, S), dtype=torch.bfloat16, device="cuda")
+        try:
+            L = torch._scaled_mm(a4, b4, sa8, sb8, out_dtype=torch.bfloat16)
+            torch.cuda.synchronize()
+        except (RuntimeError, TypeError, ValueError) as e:
+            out[str(S)] = {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+            continue
+        nv.gemm(a, sfa, b, sfb, 1.0, S, S, S, out=D)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(D.view(torch.int16), L.view(torch.int16)))
+        ms_lib = timed(lambda: torch._scaled_mm(a4, b4, sa8, sb8, out_dtype=torch.bfloat16))
+        ms_ours = timed(lambda: nv.gemm(a, sfa, b, sfb, 1.0, S, S, S, out=D))
+        tf = lambda ms: round(2.0 * S ** 3 / (ms / 1e3) / 1e12, 1)  # noqa: E731
+        out[str(S)] = {"library_ms": round(ms_lib, 4), "library_tflops": tf(ms_lib), "ours_ms": round(ms_ours, 4),
+                       "ours_tflops": tf(ms_ours), "ours_over_library": round(ms_lib / ms_ours, 3),
+                       "bit_identical_at_alpha_1": same}
+        del a, b, sfa, sfb, a4, b4, sa8, sb8, D, L
+    return {"impl": "cuBLASLt through torch._scaled_mm (FP4 x FP4, E4M3 scale per 16, FP32 accumulate, BF16 out)",
+            "torch": torch.__version__, "results": out}
+
+
 def cpu_baseline_gemm(S, target_s=12.0, max_samples=1 << 16):
     """The oracle on a bounded sample of the S^3 workload: sampled outputs, each a full
     K-length dot product of dequantised rows (float64).  Returns TFLOP/s."""
@@ -699,6 +754,7 @@ def run_ours(args):
             line["w4a16"] = bench_w4a16(peaks)
             line["llm_w4a4"] = bench_llm(peaks)
             line["producers"] = bench_producers(peaks)
+            line["cublaslt_same_operands"] = bench_cublaslt((S,))
             line["cpu_baseline"] = cpu_baseline_gemm(S)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -779,6 +835,8 @@ def run_only(args):
         out = bench_llm(peaks, tuple(int(c) for c in args.llm_configs.split(",")), shapes)
     elif args.only == "mma_ceiling":
         out = bench_mma_ceiling()
+    elif args.only == "cublaslt":
+        out = bench_cublaslt((S_MAIN, 16384))
     else:
         out = bench_producers(peaks)
     print(json.dumps({"only": args.only, "results": out}), flush=True)

@@ -587,17 +587,20 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // What bounds the tensor pipe here (measured on GB300 with MMA-only loops): one
 // 256 x 256 x 64 MMA occupies each SM of the pair for 128 cycles (16384 FP4 MACs per
 // SM per cycle, 4x the BF16 rate), and a stage needs 12 tcgen05.cp of 512-byte scale
-// atoms besides its 4 MMAs.  A tcgen05.cp blocks the warp that issues it for 64
-// cycles (about 128 while MMAs run), so one warp cannot issue a stage's copies in
-// the 512 cycles its MMAs take, and a thread that issues both copies and MMAs runs
-// at ~230 cycles per MMA.  So the copies are spread over six warps, placed on the
-// three sub-partitions that do not hold the MMA warp (one that shares it slows the
-// MMA issue), two copies per warp per stage.  They are ordered before the stage's
+// atoms besides its 4 MMAs.  How fast a warp can issue them depends on how the code
+// is written: a lone lane with operands the compiler cannot prove warp-uniform issues
+// one copy per ~64 cycles (~128 while MMAs run), a converged warp with warp-uniform
+// operands and elect.sync one per ~29 cycles.  So the MMA warp and the copy warps run
+// their loops as whole warps (values broadcast from lane 0, barrier waits by vote,
+// lane 0 elected in each tcgen05 instruction); this took the kernel from 193 to
+// 175 us at 8192^3.  The copies are spread over six warps, placed on the three
+// sub-partitions that do not hold the MMA warp, two copies per warp per stage (three
+// warps with four copies each measured 224 us).  They are ordered before the stage's
 // MMAs without waiting for their completion: each copy warp issues its copies,
 // executes tcgen05.fence::before_thread_sync and arrives on the stage's "sf"
-// barrier; the MMA thread waits for it and executes tcgen05.fence::after_thread_sync
+// barrier; the MMA warp waits for it and executes tcgen05.fence::after_thread_sync
 // before its MMAs, which places the MMAs after the copies in the tensor pipe.  The
-// MMA thread then issues the stage's four MMAs from precomputed descriptors and
+// MMA warp then issues the stage's four MMAs from precomputed descriptors and
 // releases the stage to both CTAs with a multicast commit.  Eight epilogue warps per
 // CTA drain the accumulator (128 lanes x 256 columns) into a 128-byte-swizzled BF16
 // staging tile, loading the next 32-column chunk from TMEM while converting the
@@ -830,12 +833,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader CTA)
-    if (leader && lane == 0) {
+    // The whole warp runs the loop on warp-uniform values (barrier waits by vote) and
+    // lane 0, elected in each instruction, issues.
+    if (leader) {
       griddep_wait();  // time-limited waits start once the previous grid is done
+      const uint32_t tm = warp_uniform(tmem);
+      const uint32_t sb = warp_uniform(sbase);
+      // (each barrier address rebased on the uniform shared-memory base)
+      const uint32_t u_full = sb + (bar_full - sbase), u_empty = sb + (bar_empty - sbase);
+      const uint32_t u_accf = sb + (bar_accf - sbase), u_acce = sb + (bar_acce - sbase);
+      const uint32_t u_sf = sb + (bar_sf - sbase), u_drain = sb + (bar_drain - sbase);
       // Descriptors of stage 0, K-step 0; stage s, K-step j adds s * 16 KB + j * 32 bytes
       // to the start address (16-byte units in the low bits).
-      const uint64_t adesc0 = make_sdesc(sbase + kOffA, 16, 1024, 2);
-      const uint64_t bdesc0 = make_sdesc(sbase + kOffB, 16, 1024, 2);
+      const uint64_t adesc0 = make_sdesc(sb + kOffA, 16, 1024, 2);
+      const uint64_t bdesc0 = make_sdesc(sb + kOffB, 16, 1024, 2);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
@@ -843,36 +854,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < nseg && ok; ++s) {
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
-        if (!mbar_wait_spin<true>(bar_acce, acc_phase ^ 1, abort_flag)) break;
+        if (!warp_wait_vote<true>(u_acce, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
           // The copy warps arrive only after the stage's operands landed (they wait
           // for its full barrier) and their scale copies were issued.
-          if (!mbar_wait_spin(bar_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
-          if (!mbar_wait_spin<true>(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!warp_wait_vote(u_sf + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!warp_wait_vote<true>(u_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sf_t = tmem + kTmemSF + stage * kSFSlotCols;
+          const uint32_t sf_t = tm + kTmemSF + stage * kSFSlotCols;
           const uint64_t ad = adesc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
           const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
           if (KG - kb * kStepsP >= kStepsP) {
-            tc_mma_nvf4_pair(tmem, ad, bd, kIdesc, sf_t, sf_t + kSFACols, kb != kb0 ? 1u : 0u);
+            tc_mma_nvf4_pair_elect(tm, ad, bd, kIdesc, sf_t, sf_t + kSFACols, kb != kb0 ? 1u : 0u);
 #pragma unroll
             for (int j = 1; j < kStepsP; ++j)
-              tc_mma_nvf4_pair(tmem, ad + 2 * j, bd + 2 * j, kIdesc, sf_t + 4 * j, sf_t + kSFACols + 8 * j, 1u);
+              tc_mma_nvf4_pair_elect(tm, ad + 2 * j, bd + 2 * j, kIdesc, sf_t + 4 * j, sf_t + kSFACols + 8 * j, 1u);
           } else {
             const int nk = KG - kb * kStepsP;
             for (int j = 0; j < nk; ++j)
-              tc_mma_nvf4_pair(tmem, ad + 2 * j, bd + 2 * j, kIdesc, sf_t + 4 * j, sf_t + kSFACols + 8 * j,
-                               (kb != kb0 || j != 0) ? 1u : 0u);
+              tc_mma_nvf4_pair_elect(tm, ad + 2 * j, bd + 2 * j, kIdesc, sf_t + 4 * j, sf_t + kSFACols + 8 * j,
+                                     (kb != kb0 || j != 0) ? 1u : 0u);
           }
-          tc_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+          tc_commit_pair_mc_elect(u_empty + 8 * stage, 0x3);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit_pair_mc(bar_accf, 0x3);
+        tc_commit_pair_mc_elect(u_accf, 0x3);
         acc_phase ^= 1;
       }
-      tc_commit_pair_mc(bar_drain, 0x3);  // see the teardown
+      tc_commit_pair_mc_elect(u_drain, 0x3);  // see the teardown
     }
   } else if (warp >= kSFWarp) {
     // ------------------------------------------------------------ scale copies (leader CTA)
@@ -881,9 +892,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // c (c < 4) or band (c / 4 - 1) of SFB of MMA c % 4; warp i takes the copies with
     // c % 6 == i.  The slot is free: the stage only refills (and its full barrier only
     // completes) after the MMAs that read the slot have committed.
-    const int cw = sf_warp_index(warp);
-    if (leader && lane == 0 && cw >= 0) {
+    // The whole warp runs the loop on warp-uniform values; lane 0 issues (elected).
+    const int cw = static_cast<int>(warp_uniform(static_cast<uint32_t>(sf_warp_index(warp))));
+    if (leader && cw >= 0) {
       griddep_wait();
+      const uint32_t tm = warp_uniform(tmem);
+      const uint32_t sb = warp_uniform(sbase);
+      const uint32_t u_fsf = sb + (bar_fsf - sbase), u_sf = sb + (bar_sf - sbase);
+      const uint32_t u_drain = sb + (bar_drain - sbase);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -891,29 +907,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         int t, kb0, kb1, kind;
         sched.template seg<SK>(s, t, kb0, kb1, kind);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_spin<true>(bar_fsf + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!warp_wait_vote<true>(u_fsf + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nk = min(kStepsP, KG - kb * kStepsP);
-          const uint32_t sf_t = tmem + kTmemSF + stage * kSFSlotCols;
-          const uint32_t sSFA = sbase + kOffSFA + stage * kSFABytes;
-          const uint32_t sSFB = sbase + kOffSFB + stage * kSFBBytes;
+          const uint32_t sf_t = tm + kTmemSF + stage * kSFSlotCols;
+          const uint32_t sSFA = sb + kOffSFA + stage * kSFABytes;
+          const uint32_t sSFB = sb + kOffSFB + stage * kSFBBytes;
 #pragma unroll
           for (int c = cw; c < kSFCopies; c += kSFWarps) {
             const int j = c % kStepsP, k = c / kStepsP;
             if (j < nk) {
               if (k == 0)
-                tc_cp_32x128b_warpx4_pair(sf_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+                tc_cp_32x128b_warpx4_pair_elect(sf_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
               else
-                tc_cp_32x128b_warpx4_pair(sf_t + kSFACols + 8 * j + 4 * (k - 1),
-                                          make_sdesc(sSFB + ((k - 1) * kStepsP + j) * kAtom, 0, 128, 0));
+                tc_cp_32x128b_warpx4_pair_elect(sf_t + kSFACols + 8 * j + 4 * (k - 1),
+                                                make_sdesc(sSFB + ((k - 1) * kStepsP + j) * kAtom, 0, 128, 0));
             }
           }
           tc_fence_before();
-          mbar_arrive(bar_sf + 8 * stage);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(u_sf + 8 * stage);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      tc_commit_pair_mc(bar_drain, 0x3);  // see the teardown
+      tc_commit_pair_mc_elect(u_drain, 0x3);  // see the teardown
     }
   } else {
     // ------------------------------------------------------------ epilogue (8 warps, both CTAs)

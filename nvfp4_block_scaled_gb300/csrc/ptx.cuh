@@ -154,6 +154,33 @@ __device__ __forceinline__ bool warp_wait_spin(uint32_t bar, uint32_t parity, vo
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Wait for a phase with the whole warp: every lane polls by test_wait and the warp
+// leaves the loop together on a vote, so the warp never diverges and values computed
+// after the wait stay warp-uniform (what the elect-issued tcgen05 forms need).
+// Measured in the pair GEMM's MMA and scale-copy warps: lane 0 polling with a shuffle
+// broadcast afterwards made the kernel 6 % slower than lone-lane code, this form 9 %
+// faster.  Same limits and abort protocol as mbar_wait.
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait_vote(uint32_t bar, uint32_t parity, volatile int* abort) {
+  auto done = [&] { return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity); };
+  if (__all_sync(0xffffffffu, done())) return true;
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (__all_sync(0xffffffffu, done())) return true;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitLimitNs)) {
+      if (lane_id() == 0) {
+        *abort = 1;
+        record_device_error(kDevErrTimeout);
+      }
+      return false;
+    }
+  }
+}
+
 // Wait at most `limit_ns` for a phase, ignoring the abort flag (teardown after an
 // abort: lets copies already issued land before shared memory is released).
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -486,5 +513,41 @@ __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+
+// Warp-wide forms: executed by all 32 lanes of a converged warp with warp-uniform
+// operands; elect.sync picks one lane (the lowest, lane 0) to issue.  Measured on
+// GB300: one warp issues a 32x128b.warpx4 copy every 29 cycles this way, against 63
+// when a lone lane issues it with operands the compiler cannot prove uniform (a small
+// MMA: 48 against 65 cycles).  A commit tracks the issuing lane's own operations, so
+// the commit form elects the same lane as the issue forms.
+__device__ __forceinline__ void tc_mma_nvf4_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_pair_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_mc_elect(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          bar),
+      "h"(cta_mask)
+      : "memory");
+}
+// A value the compiler can treat as uniform across the warp (broadcast from lane 0).
+__device__ __forceinline__ uint32_t warp_uniform(uint32_t v) { return __shfl_sync(0xffffffffu, v, 0); }
 
 }  // namespace nvfp4
