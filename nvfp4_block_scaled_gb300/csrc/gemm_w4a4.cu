@@ -985,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) hp[i] = __ldcg(part + i * 32);
       }
-      if (!warp_wait_spin<true>(bar_accf, acc_phase, abort_flag)) break;
+      if (!warp_wait_vote<true>(bar_accf, acc_phase, abort_flag)) break;
       tc_fence_after();
       if (SK && kind == PairSched::kHead) {
         // ---- head piece: publish the FP32 partial tile for the pair that finishes it
@@ -1018,9 +1018,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
       }
-      // Drain the accumulator in four 32-column chunks: chunk c + 1 is loaded from TMEM
-      // while chunk c is converted and staged, and the accumulator goes back to the
-      // MMA issuer as soon as the last chunk is in registers.
+      // Drain the accumulator in four 32-column chunks, two TMEM loads per wait: the
+      // first two chunks are converted and staged while nothing else is in flight, and
+      // the accumulator goes back to the MMA issuer as soon as the last two are in
+      // registers.
       const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * 128);
       auto stage_chunk = [&](uint32_t (&v)[32], int c32) {
         if (part != nullptr) {
@@ -1056,16 +1057,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
       const uint32_t box_rows = out_base + h * kOutBox + q * 32 * 128;
       uint32_t va[32], vb[32];
-      tc_ld_32x32b_x32(trow, va);
-      tc_wait_ld(va);
-      tc_ld_32x32b_x32(trow + 32, vb);
-      stage_chunk(va, 0);
-      tc_wait_ld(vb);
-      tc_ld_32x32b_x32(trow + 64, va);
-      stage_chunk(vb, 1);
-      tc_wait_ld(va);
-      tc_ld_32x32b_x32(trow + 96, vb);
-      tc_wait_ld(vb);
+      if (part == nullptr) {
+        // Two loads per wait (one TMEM round trip per 64 columns, measured 2 % faster
+        // than one per chunk): chunks 0 and 1, staged, then chunks 2 and 3.
+        tc_ld_32x32b_x32(trow, va);
+        tc_ld_32x32b_x32(trow + 32, vb);
+        tc_wait_ld(va);
+        tc_bind(vb);
+        stage_chunk(va, 0);
+        stage_chunk(vb, 1);
+        tc_ld_32x32b_x32(trow + 64, va);
+        tc_ld_32x32b_x32(trow + 96, vb);
+        tc_wait_ld(va);
+        tc_bind(vb);
+      } else {
+        // stream-K tail: the head pair's partial is added chunk by chunk
+        tc_ld_32x32b_x32(trow, va);
+        tc_wait_ld(va);
+        tc_ld_32x32b_x32(trow + 32, vb);
+        stage_chunk(va, 0);
+        tc_wait_ld(vb);
+        tc_ld_32x32b_x32(trow + 64, va);
+        stage_chunk(vb, 1);
+        tc_wait_ld(va);
+        tc_ld_32x32b_x32(trow + 96, vb);
+        tc_wait_ld(vb);
+      }
       // Accumulator read out: hand it back to the MMA issuer (before any store of this
       // tile is in flight: an arrival issued behind a TMA store was measured to reach
       // its waiter ~1 us late).

@@ -336,6 +336,19 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// Orders the uses of registers written by a tcgen05.ld after a tcgen05.wait::ld that
+// was issued for an earlier load of the same batch.
+__device__ __forceinline__ void tc_bind(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // Registers -> TMEM: thread i of the warp writes lane (warp's lane quarter) + i,
 // N consecutive 32-bit columns starting at taddr's column.
 __device__ __forceinline__ void tc_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16]) {
