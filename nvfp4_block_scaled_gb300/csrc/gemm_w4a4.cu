@@ -217,46 +217,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop on warp-uniform values (barrier waits by vote) and
+    // lane 0, elected in each instruction, issues the scale copies and the MMAs.
+    {
       griddep_wait();  // time-limited waits start once the previous grid is done
       constexpr uint32_t idesc = idesc_nvf4_m128<BN>();
+      const uint32_t tm = warp_uniform(tmem);
+      const uint32_t sb = warp_uniform(sbase);
+      const uint32_t u_full = sb + (bar_full - sbase), u_empty = sb + (bar_empty - sbase);
+      const uint32_t u_accf = sb + (bar_accf - sbase), u_acce = sb + (bar_acce - sbase);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        if (!mbar_wait(bar_acce + 8 * acc, acc_phase ^ 1, abort_flag)) break;
+        if (!warp_wait_vote(u_acce + 8 * acc, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * BN;
+        const uint32_t d_tmem = tm + acc * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
+          if (!warp_wait_vote(u_full + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const int nk = min(kKSteps, KG - kb * kKSteps);
-          const uint32_t sfa_t = tmem + C::kTmemSF + stage * (C::kSFACols + C::kSFBCols);
+          const uint32_t sfa_t = tm + C::kTmemSF + stage * (C::kSFACols + C::kSFBCols);
           const uint32_t sfb_t = sfa_t + C::kSFACols;
-          const uint32_t sA = sbase + C::kOffA + stage * C::kABytes;
-          const uint32_t sB = sbase + C::kOffB + stage * C::kBBytes;
-          const uint32_t sSFA = sbase + C::kOffSFA + stage * C::kSFABytes;
-          const uint32_t sSFB = sbase + C::kOffSFB + stage * C::kSFBBytes;
+          const uint32_t sA = sb + C::kOffA + stage * C::kABytes;
+          const uint32_t sB = sb + C::kOffB + stage * C::kBBytes;
+          const uint32_t sSFA = sb + C::kOffSFA + stage * C::kSFABytes;
+          const uint32_t sSFB = sb + C::kOffSFB + stage * C::kSFBBytes;
           for (int j = 0; j < nk; ++j) {
-            tc_cp_32x128b_warpx4(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+            tc_cp_32x128b_warpx4_elect(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
 #pragma unroll
             for (int b = 0; b < C::kBands; ++b)
-              tc_cp_32x128b_warpx4(sfb_t + 4 * (j * C::kBands + b),
-                                   make_sdesc(sSFB + (b * kKSteps + j) * kAtom, 0, 128, 0));
+              tc_cp_32x128b_warpx4_elect(sfb_t + 4 * (j * C::kBands + b),
+                                         make_sdesc(sSFB + (b * kKSteps + j) * kAtom, 0, 128, 0));
           }
           for (int j = 0; j < nk; ++j) {
             const uint64_t adesc = make_sdesc(sA + j * (kMmaK / 2), 16, 1024, 2);
             const uint64_t bdesc = make_sdesc(sB + j * (kMmaK / 2), 16, 1024, 2);
-            tc_mma_nvf4(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * j * C::kBands,
-                        (kb | j) != 0 ? 1u : 0u);
+            tc_mma_nvf4_elect(d_tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * j * C::kBands,
+                              (kb | j) != 0 ? 1u : 0u);
           }
-          tc_commit(bar_empty + 8 * stage);
+          tc_commit_elect(u_empty + 8 * stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit(bar_accf + 8 * acc);
+        tc_commit_elect(u_accf + 8 * acc);
         if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
       }
     }
@@ -425,38 +431,43 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Whole warp, warp-uniform values, barrier waits by vote, lane 0 elected to issue.
+    {
       griddep_wait();
       constexpr uint32_t idesc = idesc_nvf4_m128<BN>();
+      const uint32_t tm = warp_uniform(tmem);
+      const uint32_t sb = warp_uniform(sbase);
+      const uint32_t u_full = sb + (bar_full - sbase), u_empty = sb + (bar_empty - sbase);
+      const uint32_t u_accf = sb + (bar_accf - sbase);
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag)) break;
+        if (!warp_wait_vote(u_full + 8 * stage, phase, abort_flag)) break;
         tc_fence_after();
         const int nk = min(kKSteps, KG - kb * kKSteps);
-        const uint32_t sfa_t = tmem + C::kTmemSF + stage * (C::kSFACols + C::kSFBCols);
+        const uint32_t sfa_t = tm + C::kTmemSF + stage * (C::kSFACols + C::kSFBCols);
         const uint32_t sfb_t = sfa_t + C::kSFACols;
-        const uint32_t sA = sbase + C::kOffA + stage * C::kABytes;
-        const uint32_t sB = sbase + C::kOffB + stage * C::kBBytes;
-        const uint32_t sSFA = sbase + C::kOffSFA + stage * C::kSFABytes;
-        const uint32_t sSFB = sbase + C::kOffSFB + stage * C::kSFBBytes;
+        const uint32_t sA = sb + C::kOffA + stage * C::kABytes;
+        const uint32_t sB = sb + C::kOffB + stage * C::kBBytes;
+        const uint32_t sSFA = sb + C::kOffSFA + stage * C::kSFABytes;
+        const uint32_t sSFB = sb + C::kOffSFB + stage * C::kSFBBytes;
         for (int j = 0; j < nk; ++j) {
-          tc_cp_32x128b_warpx4(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
+          tc_cp_32x128b_warpx4_elect(sfa_t + 4 * j, make_sdesc(sSFA + j * kAtom, 0, 128, 0));
 #pragma unroll
           for (int b = 0; b < C::kBands; ++b)
-            tc_cp_32x128b_warpx4(sfb_t + 4 * (j * C::kBands + b),
-                                 make_sdesc(sSFB + (b * kKSteps + j) * kAtom, 0, 128, 0));
+            tc_cp_32x128b_warpx4_elect(sfb_t + 4 * (j * C::kBands + b),
+                                       make_sdesc(sSFB + (b * kKSteps + j) * kAtom, 0, 128, 0));
         }
         for (int j = 0; j < nk; ++j) {
           const uint64_t adesc = make_sdesc(sA + j * (kMmaK / 2), 16, 1024, 2);
           const uint64_t bdesc = make_sdesc(sB + j * (kMmaK / 2), 16, 1024, 2);
-          tc_mma_nvf4(tmem, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * j * C::kBands,
-                      (kb != kb0 || j != 0) ? 1u : 0u);
+          tc_mma_nvf4_elect(tm, adesc, bdesc, idesc, sfa_t + 4 * j, sfb_t + 4 * j * C::kBands,
+                            (kb != kb0 || j != 0) ? 1u : 0u);
         }
-        tc_commit(bar_empty + 8 * stage);
+        tc_commit_elect(u_empty + 8 * stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
-      tc_commit(bar_accf);  // also when the loop gave up: lets the epilogue proceed
+      tc_commit_elect(u_accf);  // also when the loop gave up: lets the epilogue proceed
     }
   } else {
     griddep_wait();

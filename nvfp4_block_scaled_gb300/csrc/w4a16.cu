@@ -1047,34 +1047,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop on warp-uniform values (barrier waits by vote) and
+    // lane 0, elected in each instruction, issues: 4-6 % faster than a lone lane
+    // waiting with try_wait (measured at 72, 144 and 1024 tokens).
+    {
       griddep_wait();
+      const uint32_t tm = warp_uniform(tmem);
+      const uint32_t sb = warp_uniform(sbase);
       const uint32_t idesc = idesc_bf16(128, nt_tok);
       const int n = ks1 - ks0;
-      // Descriptors of slot 0; a slot's (and a K = 16 step's) descriptor is that plus
-      // its byte offset / 16 in the start-address field (shared-memory addresses stay
-      // below 256 KB, so the 14-bit field does not overflow).  A lone issuing thread
-      // is latency-bound, so the per-MMA work is kept to a few adds.
-      const uint64_t a_desc0 = make_sdesc(sbase + L.off_a, 16, 1024, 2);
-      const uint64_t x_desc0 = make_sdesc(sbase + L.off_x, 16, 1024, 2);
+      const uint32_t u_af = sb + (a_full - sbase), u_ae = sb + (a_empty - sbase);
+      const uint32_t u_xf = sb + (x_full - sbase), u_xe = sb + (x_empty - sbase), u_acc = sb + (acc_full - sbase);
+      const uint64_t a_desc0 = make_sdesc(sb + L.off_a, 16, 1024, 2);
+      const uint64_t x_desc0 = make_sdesc(sb + L.off_x, 16, 1024, 2);
       int as = 0, xs = 0;
       uint32_t a_ph = 0, x_ph = 0;
       for (int i = 0; i < n; ++i) {
-        if (!mbar_wait(a_full + 8 * as, a_ph, abort_flag)) break;
-        if (!mbar_wait(x_full + 8 * xs, x_ph, abort_flag)) break;
+        if (!warp_wait_vote(u_af + 8 * as, a_ph, abort_flag)) break;
+        if (!warp_wait_vote(u_xf + 8 * xs, x_ph, abort_flag)) break;
         tc_fence_after();
         const uint64_t ad = a_desc0 + static_cast<uint64_t>(as * (kABytes >> 4));
         const uint64_t xd = x_desc0 + static_cast<uint64_t>(xs * (xbytes >> 4));
-        tc_mma_f16(tmem, ad, xd, idesc, i != 0 ? 1u : 0u);
-        tc_mma_f16(tmem, ad + 2, xd + 2, idesc, 1u);
-        tc_mma_f16(tmem, ad + 4, xd + 4, idesc, 1u);
-        tc_mma_f16(tmem, ad + 6, xd + 6, idesc, 1u);
-        tc_commit(a_empty + 8 * as);
-        tc_commit(x_empty + 8 * xs);
+        tc_mma_f16_elect(tm, ad, xd, idesc, i != 0 ? 1u : 0u);
+        tc_mma_f16_elect(tm, ad + 2, xd + 2, idesc, 1u);
+        tc_mma_f16_elect(tm, ad + 4, xd + 4, idesc, 1u);
+        tc_mma_f16_elect(tm, ad + 6, xd + 6, idesc, 1u);
+        tc_commit_elect(u_ae + 8 * as);
+        tc_commit_elect(u_xe + 8 * xs);
         if (++as == AS) { as = 0; a_ph ^= 1; }
         if (++xs == L.xs) { xs = 0; x_ph ^= 1; }
       }
-      tc_commit(acc_full);
+      tc_commit_elect(u_acc);
     }
   } else {
     // ------------------------------------------------------------ dequantise
