@@ -1404,6 +1404,12 @@ int gemm_choose_config(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   // when N is narrow.
   const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
   const int64_t tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
+  const int64_t tiles_pair = ((M + 255) / 256) * ((N + 255) / 256);
+  // One nearly full wave of CTA pairs (256 x 256 tiles on at least 3/4 of the pairs)
+  // beats splitting K, up to K = 8192: measured (graph replay) at M = 128, N = 17408,
+  // K = 5120 (68 tiles on 76 pairs): 13.5 us against 17.0 (split over 128 x 256 tiles)
+  // and 15.5 (over 128 x 128).  With 20 to 24 pair tiles (N = 5120, 6144) split-K wins.
+  if (K % 256 == 0 && K <= 8192 && M > 64 && N > 128 && 4 * tiles_pair >= 3 * (dev.num_sms / 2)) return 3;
   // Split K over 128 x 128 tiles unless those alone nearly fill the SMs (then over
   // 128 x 256 tiles, whose smaller split moves fewer partial sums): measured on the
   // 128-token layer shapes, e.g. 11.8 us against 17.4 us at N = K = 5120.
