@@ -333,8 +333,9 @@ nvfp4_status nvfp4_w4a16_linear(const void* x_bf16, const void* Wprep, float alp
 
 /*
  * Size in bytes of the workspace nvfp4_w4a16_linear_streamk needs on the current
- * device (two FP32 partial slots of 32 tokens x 256 rows per SM plus two tickets per
- * SM, about 64 KB per SM); 0 if no device can be queried.
+ * device: for up to 32 tokens two FP32 partial slots of 32 tokens x 256 rows and two
+ * tickets per SM, then for more tokens two slots of 128 rows x 256 tokens and one
+ * ticket per SM (about 320 KB per SM in all); 0 if no device can be queried.
  */
 size_t nvfp4_w4a16_streamk_workspace_bytes(void);
 
@@ -348,8 +349,11 @@ size_t nvfp4_w4a16_streamk_workspace_bytes(void);
  * summed through the workspace: each part stores its FP32 partial and takes a ticket,
  * and the part that takes the last ticket adds all partials in part order (so the
  * result does not depend on which part finishes last), writes y and zeroes the
- * ticket.  No block waits for another.  More than 32 tokens run the tensor-core
- * kernel of nvfp4_w4a16_linear (the workspace is not touched).
+ * ticket.  No block waits for another.  More than 32 tokens run the same scheme on
+ * the tensor-core kernel: units of (token tile of up to 256 tokens, 128 weight rows,
+ * 64 K) over one block per SM, each block dequantising its weights into shared
+ * memory for tcgen05 BF16 MMAs, with the partials and tickets in the workspace's
+ * second region.
  *
  *   x_bf16, Wprep, y_bf16, M, N, K   as nvfp4_w4a16_linear.
  *   alpha        the global scale, used when alpha_col is NULL (then finite).

@@ -840,8 +840,18 @@ __global__ void __launch_bounds__(kThreads, per_sm(8 * MT))
 
 // Two partial slots per block: [Mpad tokens][256 rows] floats, at most 2 x SMs blocks
 // of up to 16 tokens or SMs blocks of 32; then one ticket per block.
-size_t w4a16_streamk_workspace_bytes_for(int num_sms) {
+// Decode region (up to 32 tokens): two partial slots of 32 tokens x 256 rows and two
+// tickets per SM.  Tensor-core region after it (more than 32 tokens): two slots of
+// 128 rows x 256 tokens and one ticket per SM.
+constexpr int kTcSkSlotFloats = 128 * 256;  // tensor-core stream-K partial: 128 rows x up to 256 tokens
+size_t w4a16_sk_decode_bytes(int num_sms) {
   return static_cast<size_t>(2) * num_sms * skd::kSlotFloats * sizeof(float) + static_cast<size_t>(num_sms) * 8 + 256;
+}
+size_t w4a16_sk_tc_slot_bytes(int num_sms) {
+  return static_cast<size_t>(2) * num_sms * kTcSkSlotFloats * sizeof(float);
+}
+size_t w4a16_streamk_workspace_bytes_for(int num_sms) {
+  return w4a16_sk_decode_bytes(num_sms) + w4a16_sk_tc_slot_bytes(num_sms) + static_cast<size_t>(num_sms) * 4 + 256;
 }
 
 template <int MT>
@@ -1212,6 +1222,408 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ tensor-core stream-K
+//
+// More than 32 tokens with a caller workspace ([P2] Design: the persistent stream-K
+// kernel over contiguous (tile, k-tile) ranges).  The units are (token tile, 128-row
+// group, 64-K step), group-major; block b of G takes units [b U / G, (b+1) U / G).  A
+// block walks its range as segments, one per (token tile, group) it touches: the same
+// weight-chunk, x-tile, A-tile and MMA pipeline as w4a16_tc_kernel, with the rings
+// counted across segments, the accumulator drained by four epilogue warps of their
+// own after each segment.  A segment that covers its whole group goes to y; a part of
+// a split group goes to the workspace (slot 2b for the block's first segment, 2b + 1
+// for its last), and the block takes the group's ticket at the end of its range.  The
+// block taking a group's last ticket adds the parts in part order, writes y and
+// zeroes the ticket.  No block waits for another.
+constexpr int kSkEpiWarp = kFirstDeqWarp + kDeqWarps;  // 19..22: epilogue, one per TMEM lane quarter
+constexpr int kSkThreads = 32 * (kSkEpiWarp + 4);
+constexpr int kSkSlotFloats = kTcSkSlotFloats;          // partial of one group: 128 rows x up to 256 tokens
+static_assert(kSkSlotFloats >= 128 * kMaxTokens, "stream-K slot");
+
+__host__ __device__ __forceinline__ int64_t sk_unit_start(int i, int G, int64_t U) {
+  return static_cast<int64_t>(i) * U / G;
+}
+__device__ __forceinline__ int sk_cta_of(int64_t u, int G, int64_t U) {
+  int i = static_cast<int>((u * G) / U);
+  while (i + 1 < G && sk_unit_start(i + 1, G, U) <= u) ++i;
+  while (i > 0 && sk_unit_start(i, G, U) > u) --i;
+  return i;
+}
+
+__global__ void __launch_bounds__(kSkThreads, 1)
+    w4a16_tc_sk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       float alpha128, const float* __restrict__ alpha_col, __nv_bfloat16* __restrict__ y, int M,
+                       int N, int K, int nt_tok, int mt, float* __restrict__ partials, int* __restrict__ tickets) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - smem_u32(smem_raw));
+  const Layout L = layout(nt_tok);
+  const int G = gridDim.x;
+  const int KS = K / 64;
+  const int groups = N / 128;
+  const int64_t U = static_cast<int64_t>(mt) * groups * KS;
+  const int64_t u0 = sk_unit_start(blockIdx.x, G, U), u1 = sk_unit_start(blockIdx.x + 1, G, U);
+  const int xbytes = nt_tok * 128;
+
+  const uint32_t raw_full = sbase + L.off_bar;
+  const uint32_t raw_empty = raw_full + 8 * kMaxRawStages;
+  const uint32_t a_full = raw_empty + 8 * kMaxRawStages;
+  const uint32_t a_empty = a_full + 8 * kMaxAStages;
+  const uint32_t x_full = a_empty + 8 * kMaxAStages;
+  const uint32_t x_empty = x_full + 8 * kMaxXStages;
+  const uint32_t acc_full = x_empty + 8 * kMaxXStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_bar + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 8 * kNumBars + 4);
+  // (the weight ring uses RS = 2 of its kMaxRawStages barrier slots: the last one is free)
+  const uint32_t acc_empty = raw_full + 8 * (kMaxRawStages - 1);
+  const int AS = L.as;
+  const int RS = L.rs;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ncols = tmem_cols_for(nt_tok);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(raw_full + 8 * i, 1);
+      mbar_init(raw_empty + 8 * i, kDeqWarps);
+    }
+    for (int i = 0; i < AS; ++i) {
+      mbar_init(a_full + 8 * i, kDeqWarps / 2);
+      mbar_init(a_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < L.xs; ++i) {
+      mbar_init(x_full + 8 * i, 1);
+      mbar_init(x_empty + 8 * i, 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+
+  // Segment s of this block: units [su, su + n) = steps [s0, s0 + n) of (token tile, group) pg.
+  auto segment = [&](int64_t su, int64_t& pg, int& s0, int& n) {
+    pg = su / KS;
+    s0 = static_cast<int>(su - pg * KS);
+    n = static_cast<int>(min(static_cast<int64_t>(KS - s0), u1 - su));
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ weight chunks (boxes of 8 steps from s0)
+    if (lane == 0) {
+      prefetch_tensormap(&tmW);
+      int gc = 0;  // chunks issued
+      int st = 0;  // ring slot of chunk gc, and the parity of its round
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int64_t su = u0; su < u1 && ok;) {
+        int64_t pg;
+        int s0, n;
+        segment(su, pg, s0, n);
+        const int g = static_cast<int>(pg % groups);
+        for (int ci = 0; ci * kChunkKC < n; ++ci, ++gc) {
+          if (gc == RS) griddep_wait();
+          if (gc >= RS && !mbar_wait(raw_empty + 8 * st, ph ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(raw_full + 8 * st, kChunkBytes);
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + st * kChunkBytes),
+              "l"(&tmW), "r"(0), "r"(s0 + ci * kChunkKC), "r"(g * kDecodeNT), "r"(raw_full + 8 * st)
+              : "memory");
+          if (++st == RS) { st = 0; ph ^= 1; }
+        }
+        su += n;
+      }
+      if (gc <= RS) griddep_wait();
+      for (int i = gc > RS ? gc - RS : 0; i < gc; ++i)
+        mbar_wait_for(raw_full + 8 * (i % RS), (i / RS) & 1, 2000000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ x tiles
+    if (lane == 0) {
+      prefetch_tensormap(&tmX);
+      griddep_wait();
+      int gs = 0;  // steps issued
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int64_t su = u0; su < u1 && ok;) {
+        int64_t pg;
+        int s0, n;
+        segment(su, pg, s0, n);
+        const int m0 = static_cast<int>(pg / groups) * nt_tok;
+        for (int i = 0; i < n; ++i, ++gs) {
+          if (gs >= L.xs && !mbar_wait(x_empty + 8 * st, ph ^ 1, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(x_full + 8 * st, xbytes);
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + L.off_x + st * xbytes),
+              "l"(&tmX), "r"(0), "r"(m0), "r"(s0 + i), "r"(x_full + 8 * st)
+              : "memory");
+          if (++st == L.xs) { st = 0; ph ^= 1; }
+        }
+        su += n;
+      }
+      for (int i = gs > L.xs ? gs - L.xs : 0; i < gs; ++i)
+        mbar_wait_for(x_full + 8 * (i % L.xs), (i / L.xs) & 1, 2000000000ull);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issuer (whole warp, elected issue)
+    griddep_wait();
+    const uint32_t tm = warp_uniform(tmem);
+    const uint32_t sb = warp_uniform(sbase);
+    const uint32_t idesc = idesc_bf16(128, nt_tok);
+    const uint32_t u_af = sb + (a_full - sbase), u_ae = sb + (a_empty - sbase);
+    const uint32_t u_xf = sb + (x_full - sbase), u_xe = sb + (x_empty - sbase);
+    const uint32_t u_accf = sb + (acc_full - sbase), u_acce = sb + (acc_empty - sbase);
+    const uint64_t a_desc0 = make_sdesc(sb + L.off_a, 16, 1024, 2);
+    const uint64_t x_desc0 = make_sdesc(sb + L.off_x, 16, 1024, 2);
+    // ring slots and phases advance by one per step (no division on this warp's path)
+    int as = 0, xs = 0, seg = 0;
+    uint32_t a_ph = 0, x_ph = 0;
+    bool ok = true;
+    for (int64_t su = u0; su < u1 && ok; ++seg) {
+      int64_t pg;
+      int s0, n;
+      segment(su, pg, s0, n);
+      // the epilogue has drained the previous segment's accumulator
+      if (seg > 0 && !warp_wait_vote(u_acce, (seg - 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      for (int i = 0; i < n; ++i) {
+        if (!warp_wait_vote(u_af + 8 * as, a_ph, abort_flag)) { ok = false; break; }
+        if (!warp_wait_vote(u_xf + 8 * xs, x_ph, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t ad = a_desc0 + static_cast<uint64_t>(as * (kABytes >> 4));
+        const uint64_t xd = x_desc0 + static_cast<uint64_t>(xs * (xbytes >> 4));
+        tc_mma_f16_elect(tm, ad, xd, idesc, i != 0 ? 1u : 0u);
+        tc_mma_f16_elect(tm, ad + 2, xd + 2, idesc, 1u);
+        tc_mma_f16_elect(tm, ad + 4, xd + 4, idesc, 1u);
+        tc_mma_f16_elect(tm, ad + 6, xd + 6, idesc, 1u);
+        tc_commit_elect(u_ae + 8 * as);
+        tc_commit_elect(u_xe + 8 * xs);
+        if (++as == AS) { as = 0; a_ph ^= 1; }
+        if (++xs == L.xs) { xs = 0; x_ph ^= 1; }
+      }
+      tc_commit_elect(u_accf);  // also after a timed-out wait: lets the epilogue proceed
+      su += n;
+    }
+  } else if (warp < kSkEpiWarp) {
+    // ------------------------------------------------------------ dequantise
+    // Warp (p, w): n-tile w of the steps of parity p within each chunk.  Every warp
+    // waits for every chunk and releases it once, also a chunk with no step of its
+    // parity (a one-step chunk at a segment's end): the ring slot is refilled only
+    // after all sixteen warps are past the chunk.
+    griddep_wait();
+    const int w = (warp - kFirstDeqWarp) & 7;
+    const int par = (warp - kFirstDeqWarp) >> 3;
+    const int g8 = lane >> 2, t = lane & 3;
+    int rs = 0;  // chunk ring slot and the parity of its round
+    uint32_t rph = 0;
+    int gs0 = 0;  // steps before the current segment
+    // A ring position of global step `cur`, advanced by small steps (no division)
+    int cur = 0, as = 0;
+    uint32_t aph = 0;
+    auto a_slot_of = [&](int ig) {
+      while (cur < ig) {
+        ++cur;
+        if (++as == AS) { as = 0; aph ^= 1; }
+      }
+    };
+    bool ok = true;
+    for (int64_t su = u0; su < u1 && ok;) {
+      int64_t pg;
+      int s0, n;
+      segment(su, pg, s0, n);
+      for (int ci = 0; ci * kChunkKC < n && ok; ++ci) {
+        if (!warp_wait(raw_full + 8 * rs, rph, abort_flag)) { ok = false; break; }
+        const int kcn = min(kChunkKC, n - ci * kChunkKC);
+        for (int kb = par; kb < kcn; kb += 2) {
+          const int ig = gs0 + ci * kChunkKC + kb;  // global step
+          a_slot_of(ig);
+          if (ig >= AS && !warp_wait(a_empty + 8 * as, aph ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t blk = sbase + rs * kChunkBytes + (w * kChunkKC + kb) * kBlockBytes;
+          uint4 c;
+          uint2 sc;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
+                       : "r"(blk + 16 * lane));
+          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(sc.x), "=r"(sc.y) : "r"(blk + 512 + 8 * g8));
+          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+          const uint32_t a_lo = sbase + L.off_a + as * kABytes + (16 * w + g8) * 128 + 4 * t;
+          const uint32_t a_hi = a_lo + 8 * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t sword = j < 2 ? sc.x : sc.y;
+            uint32_t a[4];
+            dequant_word(words[j], scale_pair(sword, j), a);
+            const uint32_t p0 = static_cast<uint32_t>(((2 * j) ^ g8) * 16);
+            const uint32_t p1 = static_cast<uint32_t>(((2 * j + 1) ^ g8) * 16);
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_lo + p0), "r"(a[0]) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_hi + p0), "r"(a[1]) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_lo + p1), "r"(a[2]) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(a_hi + p1), "r"(a[3]) : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(a_full + 8 * as);
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(raw_empty + 8 * rs);
+        if (++rs == RS) { rs = 0; rph ^= 1; }
+      }
+      gs0 += n;
+      su += n;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 19-22)
+    griddep_wait();
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = 32 * q + lane;
+    const int nchunks = (nt_tok + 31) / 32;
+    int seg = 0;
+    for (int64_t su = u0; su < u1; ++seg) {
+      int64_t pg;
+      int s0, n;
+      segment(su, pg, s0, n);
+      if (!warp_wait(acc_full, seg & 1, abort_flag)) break;
+      tc_fence_after();
+      const int g = static_cast<int>(pg % groups);
+      const int m0 = static_cast<int>(pg / groups) * nt_tok;
+      const int mv = min(nt_tok, M - m0);
+      const bool whole = s0 == 0 && n == KS;
+      const float sc = alpha_col != nullptr ? alpha_col[g * 128 + row] * 128.0f : alpha128;
+      // slot of a split part: this block's first segment or its last
+      float4* dst = reinterpret_cast<float4*>(partials) +
+                    (static_cast<size_t>(2 * blockIdx.x + (su == u0 ? 0 : 1)) * kSkSlotFloats) / 4;
+#pragma unroll 1
+      for (int c = 0; c < nchunks; ++c) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, v);
+        tc_wait_ld(v);
+        if (whole) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int tok = 32 * c + jj;
+            if (tok < mv)
+              y[static_cast<size_t>(m0 + tok) * N + static_cast<size_t>(g) * 128 + row] =
+                  __float2bfloat16_rn(__uint_as_float(v[jj]) * sc);
+          }
+        } else {
+          // [lane quarter][32-token chunk][float4 i][lane]: whole 512-byte warp stores
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(dst + ((q * nchunks + c) * 8 + i) * 32 + lane,
+                   make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                               __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+        }
+      }
+      if (!whole) __threadfence();  // the part is visible at GPU scope before the block's ticket
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      su += n;
+    }
+  }
+
+  // ------------------------------------------------------------ tickets of split groups
+  tc_fence_before();
+  __syncthreads();
+  griddep_wait();  // every thread writes y below
+  // Every role is done and no copy is in flight: the ring's first bytes hold the flags
+  // and then the slot of every part of the group being summed.
+  int* last_flag = reinterpret_cast<int*>(smem);  // [2]
+  int* part_slot = last_flag + 4;                 // [parts], at most one per block
+  if (threadIdx.x < 2) {
+    last_flag[threadIdx.x] = 0;
+    // part 0: the group of the range's first unit, part 1: that of its last unit
+    const int64_t su = threadIdx.x == 0 ? u0 : u1 - 1;
+    const int64_t pg = su / KS;
+    const int64_t gu0 = pg * KS, gu1 = gu0 + KS;
+    const bool split = u0 > gu0 || u1 < gu1;
+    const bool distinct = threadIdx.x == 0 || (u0 / KS) != pg;
+    if (u1 > u0 && split && distinct && !*abort_flag) {
+      const int first = sk_cta_of(gu0, G, U), last = sk_cta_of(gu1 - 1, G, U);
+      int old;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(tickets + first) : "memory");
+      if (old == last - first) {
+        tickets[first] = 0;
+        last_flag[threadIdx.x] = 1;
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    if (!last_flag[which]) continue;
+    // This block took the group's last ticket: add the parts in part order.
+    const int64_t pg = (which == 0 ? u0 : u1 - 1) / KS;
+    const int64_t gu0 = pg * KS;
+    const int first = sk_cta_of(gu0, G, U), last = sk_cta_of(gu0 + KS - 1, G, U);
+    const int g = static_cast<int>(pg % groups);
+    const int m0 = static_cast<int>(pg / groups) * nt_tok;
+    const int mv = min(nt_tok, M - m0);
+    const int nchunks = (nt_tok + 31) / 32;
+    for (int p = first + static_cast<int>(threadIdx.x); p <= last; p += kSkThreads)
+      part_slot[p - first] = 2 * p + (sk_unit_start(p, G, U) >= gu0 ? 0 : 1);
+    __syncthreads();
+    // One float4 of the slot layout per thread and pass ([lane quarter][32-token
+    // chunk][float4 i][lane]).  The sum is bound by L2 latency: every thread of the
+    // block takes part, each with up to eight loads in flight (one load at a time
+    // measured ~12 us for five parts of 48 KB).
+    const int nf4 = 4 * nchunks * 8 * 32;
+    const int P = last - first + 1;
+    const float4* part4 = reinterpret_cast<const float4*>(partials);
+#pragma unroll 2
+    for (int e = threadIdx.x; e < nf4; e += kSkThreads) {
+      const int ln = e & 31, i = (e >> 5) & 7, qc = e >> 8;
+      const int q = qc / nchunks, c = qc - q * nchunks;
+      const int tok0 = 32 * c + 4 * i;
+      if (tok0 >= mv) continue;
+      const int row = 32 * q + ln;
+      // up to eight parts' loads in flight at once, then added in part order
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p0 = 0; p0 < P; p0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (p0 + k < P) v[k] = __ldcg(part4 + static_cast<size_t>(part_slot[p0 + k]) * (kSkSlotFloats / 4) + e);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (p0 + k < P) {
+            sum.x += v[k].x;
+            sum.y += v[k].y;
+            sum.z += v[k].z;
+            sum.w += v[k].w;
+          }
+        }
+      }
+      const float sc = alpha_col != nullptr ? alpha_col[g * 128 + row] * 128.0f : alpha128;
+      const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (tok0 + k < mv)
+          y[static_cast<size_t>(m0 + tok0 + k) * N + static_cast<size_t>(g) * 128 + row] =
+              __float2bfloat16_rn(vals[k] * sc);
+    }
+    __syncthreads();  // part_slot is rewritten for the next group
+  }
+  if (warp == 2) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
 }  // namespace tcw
 
 // Split count S (cluster size) and token-tile width for the tensor-core path.  A
@@ -1359,11 +1771,66 @@ nvfp4_status launch_w4a16_linear(const void* x, const void* Wprep, float alpha, 
 
 size_t w4a16_streamk_workspace_bytes(const DeviceInfo& dev) { return w4a16_streamk_workspace_bytes_for(dev.num_sms); }
 
+// More than 32 tokens with the workspace: tensor-core stream-K over (token tile,
+// 128-row group, 64-K step) units, one block per SM (or per unit, if fewer).
+nvfp4_status launch_tc_sk(const void* x, const void* Wprep, float alpha128, const float* alpha_col, void* y,
+                          int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t stream, const DeviceInfo& dev) {
+  auto kern = tcw::w4a16_tc_sk_kernel;
+  static PerDeviceOnce setup;
+  const int d = dev.device < 64 ? dev.device : 63;
+  if (!setup.get(d, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(dev.max_smem_optin)) == cudaSuccess
+                   ? 1
+                   : 0;
+      }))
+    return NVFP4_ERR_CUDA;
+  const int mt = static_cast<int>((M + tcw::kMaxTokens - 1) / tcw::kMaxTokens);  // token tiles
+  const int per = static_cast<int>((M + mt - 1) / mt);
+  const int nt = ((per + 15) / 16) * 16;
+  const tcw::Layout L = tcw::layout(nt);
+  if (L.rs < 2 || L.rs >= tcw::kMaxRawStages || L.xs < 3 || static_cast<size_t>(L.total) > dev.max_smem_optin)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  const int64_t U = static_cast<int64_t>(mt) * (N / 128) * (K / 64);
+  const int G = static_cast<int>(U < dev.num_sms ? U : dev.num_sms);
+  CUtensorMap tmW, tmX;
+  nvfp4_status st = encode_tmap_wprep(&tmW, Wprep, N, K);
+  if (st == NVFP4_OK) st = encode_tmap_x_blocks(&tmX, x, M, K, static_cast<uint32_t>(nt), 1);
+  if (st != NVFP4_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(ws) + w4a16_sk_decode_bytes(dev.num_sms);
+  float* partials = reinterpret_cast<float*>(base);
+  int* tickets = reinterpret_cast<int*>(base + w4a16_sk_tc_slot_bytes(dev.num_sms));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G, 1, 1);
+  cfg.blockDim = dim3(tcw::kSkThreads, 1, 1);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return from_cuda(cudaLaunchKernelEx(&cfg, kern, tmW, tmX, alpha128, alpha_col, static_cast<__nv_bfloat16*>(y),
+                                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), nt, mt, partials,
+                                      tickets));
+}
+
 nvfp4_status launch_w4a16_linear_streamk(const void* x, const void* Wprep, float alpha, const float* alpha_col,
                                          void* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t stream,
                                          const DeviceInfo& dev) {
-  // More than 32 tokens: the tensor-core kernel, which needs no workspace.
-  if (M > skd::kMaxTokens) return launch_w4a16_linear(x, Wprep, alpha, alpha_col, y, M, N, K, stream, dev);
+  // More than 32 tokens: the tensor-core kernels.  Stream-K pays where the tile grid
+  // of the cluster-split kernel (token tiles x 128-row groups) leaves most of a wave
+  // empty; elsewhere its fix-up (one block adding a split group's partials at the end,
+  // ~5 us per group at 72 tokens) costs more than the balance gains.  Measured (graph
+  // replay): 5120 x 17408, 1024 tokens 195.8 -> 153.8 us; 5120 x 5120, 1024 tokens
+  // 68.7 -> 67.3 us; 17408 x 5120, 1024 tokens 164.7 -> 185.3 us; up to 256 tokens
+  // stream-K measured 0.49-0.94 of the cluster-split kernel.
+  if (M > skd::kMaxTokens) {
+    const int64_t tiles = ((M + tcw::kMaxTokens - 1) / tcw::kMaxTokens) * (N / 128);
+    if (M > tcw::kMaxTokens && 4 * tiles < 5 * static_cast<int64_t>(dev.num_sms))
+      return launch_tc_sk(x, Wprep, alpha * 128.0f, alpha_col, y, M, N, K, ws, stream, dev);
+    return launch_w4a16_linear(x, Wprep, alpha, alpha_col, y, M, N, K, stream, dev);
+  }
   const float alpha128 = alpha * 128.0f;
   CUtensorMap tmW4, tmW1, tmX;
   nvfp4_status st = encode_tmap_wprep(&tmW4, Wprep, N, K, skd::kStageBlocks, skd::kNT);

@@ -163,16 +163,92 @@ def test_chain_waits_for_the_previous_call():
     assert torch.equal(y2.view(torch.int16), want2.view(torch.int16))
 
 
-def test_more_than_32_tokens_runs_the_tensor_core_kernel():
-    M, N, K = 72, 256, 512
-    x = dev_bf16(G.bf16_normal(M, K, 3, "x"))
-    W, SW = _weights(N, K, 3)
+def _tc_tickets_zero(ws):
+    # the tensor-core tickets (one per SM) follow the decode region and the 2 x SMs
+    # tensor-core partial slots of 128 x 256 floats
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    off = (2 * sms * 32 * 256 * 4 + sms * 8 + 256) + 2 * sms * 128 * 256 * 4
+    return bool((ws[off:off + 4 * sms] == 0).all())
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (33, 256, 512),      # up to 256 tokens: the cluster-split tensor-core kernel
+    (72, 384, 1280),
+    (144, 1024, 2304),
+    (256, 640, 4096),
+    (300, 512, 1024),    # stream-K: two token tiles of 160 (150 valid each), 16 x 8 units
+    (1024, 256, 2048),   # stream-K: four token tiles, 256 units
+    (520, 1152, 768),    # stream-K: three token tiles of 176 (168 valid in the last), ragged shares
+    (2048, 640, 4096),   # stream-K: eight token tiles, 2560 units on the SMs
+])
+def test_tensor_core_streamk(M, N, K):
+    x = G.bf16_normal(M, K, 50 + M, "x")
+    W, SW = _weights(N, K, 50 + M)
+    alpha = 0.375
     wp = nv.w4a16_prepare(dev(W), dev(SW))
     ws = _ws()
-    a = nv.w4a16_linear_streamk(x, wp, 0.75, N, ws)
-    b = nv.w4a16_linear(x, wp, 0.75, N)
+    y = nv.w4a16_linear_streamk(dev_bf16(x), wp, alpha, N, ws)
     torch.cuda.synchronize()
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert nv.device_error() == 0
+    assert _tc_tickets_zero(ws) and _tickets_zero(ws)
+    ref, abs_sum = O.w4a16_linear(x, W, SW, alpha)
+    assert_within(host_f64(y), ref, abs_sum, alpha, f"tensor-core stream-K {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(72, 17408, 5120), (144, 5120, 17408), (1024, 5120, 5120)])
+def test_tensor_core_streamk_layer_shapes(M, N, K):
+    x = G.bf16_normal(M, K, 22, "x")
+    w = G.bf16_normal(N, K, 22, "w", 0.02)
+    g = O.global_scale(w)
+    W, SW = O.quantize(w, g)
+    wp = nv.w4a16_prepare(dev(W), dev(SW))
+    ws = _ws()
+    y = nv.w4a16_linear_streamk(dev_bf16(x), wp, g, N, ws)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert _tc_tickets_zero(ws)
+    rows, cols = sample_points(M, N, 1024)
+    ref, abs_sum = O.w4a16_linear_at(x, W, SW, g, rows, cols)
+    got = host_f64(y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()])
+    assert_within(got, ref, abs_sum, g, f"tensor-core stream-K {M}x{N}x{K} samples")
+    for r0, r1, c0, c1 in corner_tiles(M, N):
+        ref, abs_sum = O.w4a16_linear(x[r0:r1], W[c0:c1], SW[c0:c1], g)
+        assert_within(host_f64(y[r0:r1, c0:c1]), ref, abs_sum, g, f"tensor-core stream-K tile {(r0, c0)}")
+
+
+def test_tensor_core_streamk_colscale_and_repeats():
+    M, N, K = 600, 640, 2304  # three token tiles of 208 x 5 groups: the stream-K kernel
+    x = G.bf16_normal(M, K, 8, "x")
+    W, SW = _weights(N, K, 8)
+    acol = (np.random.default_rng(8).random(N) * 2 - 0.5).astype(np.float32)
+    wp = nv.w4a16_prepare(dev(W), dev(SW))
+    ws = _ws()
+    xd = dev_bf16(x)
+    ac = dev(acol)
+    y1 = nv.w4a16_linear_streamk(xd, wp, 0.0, N, ws, alpha_col=ac)
+    y2 = nv.w4a16_linear_streamk(xd, wp, 0.0, N, ws, alpha_col=ac)
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    ref, sabs = O.w4a16_linear_colscale(x, W, SW, acol)
+    assert_within(host_f64(y1), ref, sabs, 1.0, "tensor-core stream-K colscale")
+    # graph replay of three calls: the same bits, tickets back at zero
+    y = torch.empty_like(y1)
+    gr = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(gr, stream=s):
+            for _ in range(3):
+                nv.w4a16_linear_streamk(xd, wp, 0.0, N, ws, alpha_col=ac, out=y, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        y.zero_()
+        gr.replay()
+    torch.cuda.synchronize()
+    assert nv.device_error() == 0
+    assert _tc_tickets_zero(ws)
+    assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
 
 
 def test_workspace_checks():
