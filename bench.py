@@ -331,8 +331,9 @@ W4A16_M = (1, 8, 32, 72, 144, 1024)
 
 def bench_w4a16(peaks, shapes=None):
     """W4A16 decode: weight GB/s over CUDA-graph replay of rotated weight copies, for
-    nvfp4_w4a16_linear and, up to 32 tokens, nvfp4_w4a16_linear_streamk (keys
-    prefixed streamk_).
+    nvfp4_w4a16_linear and nvfp4_w4a16_linear_streamk (keys prefixed streamk_) up to
+    32 tokens and where the stream-K entry takes its tensor-core stream-K kernel
+    (more than 256 tokens on a tile grid of less than 1.25 waves).
     shapes: list of (N, K, [M...]); default every (N, K) of W4A16_NK with every M of W4A16_M."""
     import numpy as np
     import torch
@@ -357,7 +358,9 @@ def bench_w4a16(peaks, shapes=None):
             y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             alg_bytes = wbytes + 2 * M * K + 2 * M * N
             calls = {"": lambda w, s=None: nv.w4a16_linear(x, w, 1.0, N, out=y, stream=s)}
-            if M <= 32:
+            tiles = ((M + 255) // 256) * (N // 128)
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            if M <= 32 or (M > 256 and 4 * tiles < 5 * sms):
                 calls["streamk_"] = lambda w, s=None: nv.w4a16_linear_streamk(x, w, 1.0, N, sk_ws, out=y, stream=s)
             cell = {}
             for prefix, call in calls.items():

@@ -397,7 +397,7 @@ def w4a16_streamk_workspace_bytes() -> int:
 
 
 def w4a16_linear_streamk(x, Wprep, alpha: float, N: int, workspace, alpha_col=None, out=None, stream=None):
-    """nvfp4_w4a16_linear_streamk: the decode work split evenly over the SMs; workspace
+    """nvfp4_w4a16_linear_streamk: the work split evenly over the SMs; workspace
     is a zero-filled uint8 device tensor of w4a16_streamk_workspace_bytes() bytes."""
     import torch
 
