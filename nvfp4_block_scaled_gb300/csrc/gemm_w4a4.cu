@@ -618,6 +618,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // current one; the accumulator is released as soon as the last chunk is in
 // registers (it is single-buffered: two 256-column accumulators would leave no TMEM
 // columns for the scale slots), and D goes out with TMA stores.
+//
+// Tile schedules: static (pair p takes tiles p, p + P, ... of the grouped raster),
+// stream-K (pair_sched.h), or cluster launch control ([P1] Appendix): the grid holds
+// one cluster per tile, a running pair starts with its own tile and then cancels
+// pending clusters and takes theirs.  Warp 13 (otherwise idle) of the leader issues
+// clusterlaunchcontrol.try_cancel with the response multicast to both CTAs into a
+// two-slot ring once every consuming role (27 warps or threads over the pair) has
+// read the slot's previous response; the follower's warp 13 arms its own barrier for
+// each response.  Measured on GB300 against the static schedule: no gain (8192^3
+// 177.9 against 172.7 us; 1024 x 5120 x 17408 59.1 against 58.0), so it is an
+// explicit configuration, not the automatic choice.
 namespace pair {
 
 constexpr int kStages = 5;
@@ -649,9 +660,12 @@ constexpr int kOffSFB = kOffSFA + kStages * kSFABytes;
 constexpr int kOffOut = kOffSFB + kStages * kSFBBytes;  // 2 boxes of 128 rows x 128 B (64 bf16 columns)
 constexpr int kOutBox = 128 * 128;
 constexpr int kOffBar = kOffOut + 2 * kOutBox;
-constexpr int kNumBars = 4 * kStages + 5;
+constexpr int kClcSlots = 2;          // CLC response ring
+constexpr int kClcConsumers = 17 + 10; // leader: 2 producers, MMA, 6 copy, 8 epilogue warps; follower: 2 + 8
+constexpr int kNumBars = 4 * kStages + 5 + 2 * kClcSlots;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kOffResp = (kOffMisc + 16 + 15) / 16 * 16;
+constexpr int kSmemBytes = kOffResp + 16 * kClcSlots + 1024;
 static_assert(kOffOut % 1024 == 0 && kOffB % 1024 == 0, "swizzled tiles must be 1024-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr int kTmemCols = 512;
@@ -694,7 +708,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, volatile int* ab
 
 // SK: the stream-K schedule is compiled in (the data-parallel instantiation carries
 // none of its code or registers).
-template <bool SK>
+template <bool SK, bool CLC = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -712,6 +726,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_seen = bar_pub + 8;                // stream-K: the head partial of the tail is ready
   const uint32_t bar_fsf = bar_seen + 8;                // both CTAs' scale atoms of the stage (leader's copy)
   const uint32_t bar_drain = bar_fsf + 8 * kStages;     // every tcgen05 op of the launch has completed
+  const uint32_t bar_clcf = bar_drain + 8;              // CLC response of a ring slot has landed
+  const uint32_t bar_clce = bar_clcf + 8 * kClcSlots;   // every consumer has read it (leader's copy is used)
+  const uint32_t resp0 = sbase + kOffResp;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
 
@@ -734,6 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) mbar_init(bar_sf + 8 * s, kSFWarps);
     mbar_init(bar_pub, kEpiWarps);  // each used at most once per launch (phase 0)
     mbar_init(bar_seen, 1);
+    for (int s = 0; s < kClcSlots; ++s) {
+      mbar_init(bar_clcf + 8 * s, 1);
+      mbar_init(bar_clce + 8 * s, kClcConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -759,6 +780,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   sched.init(pair_id, num_pairs, num_tiles, KB, SK ? 1 : 0);
   const int nseg = sched.count();
 
+  // Tile i of this pair's sequence: the static schedule, or (CLC) the pair's own tile
+  // and then the tiles of the clusters it cancelled.  Every consuming role reads each
+  // CLC response once, in order, and releases its ring slot.
+  auto clc_query = [&](uint32_t addr, int& tile) -> bool {
+    uint32_t ok = 0;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%1];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr)
+        : "memory");
+    if (ok) {
+      uint32_t x;
+      asm volatile(
+          "{\n\t.reg .b128 r;\n\t"
+          "ld.shared.b128 r, [%1];\n\t"
+          "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+          : "=r"(x)
+          : "r"(addr)
+          : "memory");
+      tile = static_cast<int>(x >> 1);
+    }
+    return ok != 0;
+  };
+  auto clc_next = [&](int i, bool warp_wide) -> int {
+    const int slot = i & (kClcSlots - 1);
+    const uint32_t ph = static_cast<uint32_t>(i / kClcSlots) & 1u;
+    const bool got = warp_wide ? warp_wait_vote<true>(bar_clcf + 8 * slot, ph, abort_flag)
+                               : mbar_wait_spin<true>(bar_clcf + 8 * slot, ph, abort_flag);
+    int t = -1;
+    if (got && !clc_query(resp0 + 16 * slot, t)) t = -1;
+    if (warp_wide) __syncwarp();
+    if (!warp_wide || lane == 0) {
+      if (leader) mbar_arrive(bar_clce + 8 * slot);
+      else mbar_arrive_cluster(map_to_rank(bar_clce + 8 * slot, 0));
+    }
+    return t;
+  };
+  auto next_seg = [&](int s, int& t, int& kb0, int& kb1, int& kind, bool warp_wide) -> bool {
+    if (!CLC) {
+      if (s >= nseg) return false;
+      sched.template seg<SK>(s, t, kb0, kb1, kind);
+      return true;
+    }
+    t = s == 0 ? static_cast<int>(blockIdx.x >> 1) : clc_next(s - 1, warp_wide);
+    kb0 = 0;
+    kb1 = KB;
+    kind = PairSched::kFull;
+    return t >= 0;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer of B (both CTAs)
     // Issuing a tiled TMA load takes the issuing thread ~140 cycles, so one thread
@@ -776,9 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int issued = 0;
-      for (int s = 0; s < nseg && ok; ++s) {
+      for (int s = 0; ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.template seg<SK>(s, t, kb0, kb1, kind);
+        if (!next_seg(s, t, kb0, kb1, kind, false)) break;
         int mt, nt;
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int b_row = nt * 256 + static_cast<int>(rank) * 128;
@@ -826,9 +900,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int s = 0; s < nseg && ok; ++s) {
+      for (int s = 0; ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.template seg<SK>(s, t, kb0, kb1, kind);
+        if (!next_seg(s, t, kb0, kb1, kind, false)) break;
         int mt, nt;
         tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
         const int a_row = mt * 256 + static_cast<int>(rank) * 128;
@@ -862,9 +936,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int s = 0; s < nseg && ok; ++s) {
+      for (int s = 0; ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.template seg<SK>(s, t, kb0, kb1, kind);
+        if (!next_seg(s, t, kb0, kb1, kind, true)) break;
         if (!warp_wait_vote<true>(u_acce, acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -905,7 +979,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // completes) after the MMAs that read the slot have committed.
     // The whole warp runs the loop on warp-uniform values; lane 0 issues (elected).
     const int cw = static_cast<int>(warp_uniform(static_cast<uint32_t>(sf_warp_index(warp))));
-    if (leader && cw >= 0) {
+    if (CLC && warp == kSFWarp + 3) {
+      // CLC scheduler: the leader cancels one pending cluster per ring slot once every
+      // consumer has read the slot's previous response (multicast to both CTAs); the
+      // follower arms its own barrier for each response.  Stops after a response that
+      // cancelled nothing.
+      if (lane == 0) {
+        for (int i = 0;; ++i) {
+          const int slot = i & (kClcSlots - 1);
+          const uint32_t ph = static_cast<uint32_t>(i / kClcSlots) & 1u;
+          if (leader && i >= kClcSlots && !mbar_wait_spin<true>(bar_clce + 8 * slot, ph ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(bar_clcf + 8 * slot, 16);
+          if (leader)
+            asm volatile(
+                "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 [%0], [%1];" ::"r"(
+                    resp0 + 16 * slot),
+                "r"(bar_clcf + 8 * slot)
+                : "memory");
+          if (!mbar_wait_spin<true>(bar_clcf + 8 * slot, ph, abort_flag)) break;
+          int t;
+          if (!clc_query(resp0 + 16 * slot, t)) break;
+        }
+      }
+    } else if (leader && cw >= 0) {
       griddep_wait();
       const uint32_t tm = warp_uniform(tmem);
       const uint32_t sb = warp_uniform(sbase);
@@ -914,9 +1010,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int s = 0; s < nseg && ok; ++s) {
+      for (int s = 0; ok; ++s) {
         int t, kb0, kb1, kind;
-        sched.template seg<SK>(s, t, kb0, kb1, kind);
+        if (!next_seg(s, t, kb0, kb1, kind, true)) break;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!warp_wait_vote<true>(u_fsf + 8 * stage, phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -974,9 +1070,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // accesses.
     const size_t slot_f4 = 128 * 256 / 4;
     const int ew = warp - kFirstEpiWarp;           // epilogue warp 0..7
-    for (int s = 0; s < nseg; ++s) {
+    for (int s = 0;; ++s) {
       int t, kb0, kb1, kind;
-      sched.template seg<SK>(s, t, kb0, kb1, kind);
+      if (!next_seg(s, t, kb0, kb1, kind, true)) break;
       int mt, nt;
       tile_coords(t, tiles_m, tiles_n, group_n, mt, nt);
       const float4* part = nullptr;  // the head pair's partial of this tile (tail piece)
@@ -1151,6 +1247,7 @@ constexpr ConfigEntry kConfigs[] = {
     {"2cta_256x256_k256x4 (K % 256 == 0; other K run 1cta_128x256)", 256},
     {"1cta_128x256_splitk (K split over a cluster of up to 8 CTAs, fixed-order DSMEM reduction)", 256},
     {"1cta_128x128_splitk (K split over a cluster of up to 8 CTAs, fixed-order DSMEM reduction)", 128},
+    {"2cta_256x256_k256x4_clc (CTA pairs, dynamic tile scheduling by cluster launch control)", 256},
 };
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 
@@ -1284,6 +1381,8 @@ int pair_slots(const DeviceInfo& dev) {
     auto kern = pair::gemm_nvf4_pair_kernel<false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(pair::gemm_nvf4_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(pair::gemm_nvf4_pair_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair::kSmemBytes) != cudaSuccess)
       return -1;
     cudaLaunchConfig_t qc = {};
@@ -1315,7 +1414,7 @@ size_t streamk_bytes(int pairs) { return streamk_flags_bytes(pairs) + static_cas
 // the data-parallel schedule.
 nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, float alpha,
                       void* D, int64_t M, int64_t N, int64_t K, cudaStream_t stream, const DeviceInfo& dev,
-                      bool streamk = false, void* ws = nullptr, int b_shift = 0) {
+                      bool streamk = false, void* ws = nullptr, int b_shift = 0, bool clc = false) {
   const int slots = pair_slots(dev);
   if (slots < 0) return NVFP4_ERR_CUDA;
   CUtensorMap ta, tb, tsfa, tsfb, td;
@@ -1347,7 +1446,7 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
     const int64_t sk_cost = whole * KB + (units + slots - 1) / slots + kStreamKFixupKB;
     use_sk = sk_cost < waves * KB ? 1 : 0;
   }
-  const int pairs = use_sk ? slots : (num_tiles < slots ? num_tiles : slots);
+  const int pairs = clc ? num_tiles : use_sk ? slots : (num_tiles < slots ? num_tiles : slots);
   const int group_n = tiles_n < 8 ? tiles_n : 8;
   uint32_t* flags = use_sk ? static_cast<uint32_t*>(ws) : nullptr;
   float* part = use_sk ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + streamk_flags_bytes(slots)) : nullptr;
@@ -1364,7 +1463,8 @@ nvfp4_status run_pair(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, co
   set_programmatic(attr[1]);
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  auto kern = use_sk ? pair::gemm_nvf4_pair_kernel<true> : pair::gemm_nvf4_pair_kernel<false>;
+  auto kern = clc ? pair::gemm_nvf4_pair_kernel<false, true>
+                 : use_sk ? pair::gemm_nvf4_pair_kernel<true> : pair::gemm_nvf4_pair_kernel<false>;
   return from_cuda(cudaLaunchKernelEx(&cfg, kern, ta, tb, tsfa, tsfb, td, alpha, static_cast<int>(K), tiles_m,
                                       tiles_n, group_n, part, flags, b_shift));
 }
@@ -1445,6 +1545,9 @@ nvfp4_status launch_gemm(int config, const uint8_t* A, const uint8_t* SFA, const
       return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, false, nullptr, b_shift);
     case 4: return run_splitk<256, 3>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
     case 5: return run_splitk<128, 4>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
+    case 6:
+      if (K % 256 != 0) return run<256, 3, 1>(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, b_shift);
+      return run_pair(A, SFA, B, SFB, alpha, D, M, N, K, stream, dev, false, nullptr, b_shift, true);
     default: return NVFP4_ERR_INVALID_ARG;
   }
 }

@@ -394,3 +394,20 @@ def test_weights_written_by_the_kernel_just_before(M, N, K, config):
             check_sampled(Ah, SFAh, Bh, SFBh, alpha, D, M, N, 512, f"weights just written {M}x{N}x{K}")
         assert torch.equal(D.view(torch.int16), want.view(torch.int16)), f"iteration {it}"
     assert nv.device_error() == 0
+
+
+def _config_index(tag):
+    return 1 + next(i for i, n in enumerate(nv.gemm_configs()) if tag in n)
+
+
+def test_clc_schedule_matches_static_pairs():
+    # 12 x 12 = 144 tiles of 256 x 256 for ~76 co-resident CTA pairs: the first clusters
+    # cancel pending ones and take their tiles ([P1] Appendix, cluster launch control).
+    # Each tile is computed the same way under either schedule: identical bits.
+    M = N = 3072
+    K = 512
+    A, SFA, B, SFB = G.gemm_square_inputs(M, N, K, seed=5)
+    D_static = run_gemm(A, SFA, B, SFB, 0.5, M, N, K, config=_config_index("2cta_256x256_k256x4 ("))
+    D_clc = run_gemm(A, SFA, B, SFB, 0.5, M, N, K, config=_config_index("clc"))
+    assert torch.equal(D_static.view(torch.int16), D_clc.view(torch.int16))
+    check_sampled(A, SFA, B, SFB, 0.5, D_clc, M, N, 512, "CLC 3072x3072x512")
