@@ -27,6 +27,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "sk_units.h"
 #include "ptx.cuh"
 
 namespace nvfp4 {
@@ -1241,15 +1242,7 @@ constexpr int kSkThreads = 32 * (kSkEpiWarp + 4);
 constexpr int kSkSlotFloats = kTcSkSlotFloats;          // partial of one group: 128 rows x up to 256 tokens
 static_assert(kSkSlotFloats >= 128 * kMaxTokens, "stream-K slot");
 
-__host__ __device__ __forceinline__ int64_t sk_unit_start(int i, int G, int64_t U) {
-  return static_cast<int64_t>(i) * U / G;
-}
-__device__ __forceinline__ int sk_cta_of(int64_t u, int G, int64_t U) {
-  int i = static_cast<int>((u * G) / U);
-  while (i + 1 < G && sk_unit_start(i + 1, G, U) <= u) ++i;
-  while (i > 0 && sk_unit_start(i, G, U) > u) --i;
-  return i;
-}
+// (unit ranges: csrc/sk_units.h, shared with a host-side test)
 
 __global__ void __launch_bounds__(kSkThreads, 1)
     w4a16_tc_sk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -1263,7 +1256,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int KS = K / 64;
   const int groups = N / 128;
   const int64_t U = static_cast<int64_t>(mt) * groups * KS;
-  const int64_t u0 = sk_unit_start(blockIdx.x, G, U), u1 = sk_unit_start(blockIdx.x + 1, G, U);
+  const int64_t u0 = sku::unit_start(blockIdx.x, G, U), u1 = sku::unit_start(blockIdx.x + 1, G, U);
   const int xbytes = nt_tok * 128;
 
   const uint32_t raw_full = sbase + L.off_bar;
@@ -1552,7 +1545,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const bool split = u0 > gu0 || u1 < gu1;
     const bool distinct = threadIdx.x == 0 || (u0 / KS) != pg;
     if (u1 > u0 && split && distinct && !*abort_flag) {
-      const int first = sk_cta_of(gu0, G, U), last = sk_cta_of(gu1 - 1, G, U);
+      const int first = sku::cta_of(gu0, G, U), last = sku::cta_of(gu1 - 1, G, U);
       int old;
       asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(tickets + first) : "memory");
       if (old == last - first) {
@@ -1568,13 +1561,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // This block took the group's last ticket: add the parts in part order.
     const int64_t pg = (which == 0 ? u0 : u1 - 1) / KS;
     const int64_t gu0 = pg * KS;
-    const int first = sk_cta_of(gu0, G, U), last = sk_cta_of(gu0 + KS - 1, G, U);
+    const int first = sku::cta_of(gu0, G, U), last = sku::cta_of(gu0 + KS - 1, G, U);
     const int g = static_cast<int>(pg % groups);
     const int m0 = static_cast<int>(pg / groups) * nt_tok;
     const int mv = min(nt_tok, M - m0);
     const int nchunks = (nt_tok + 31) / 32;
     for (int p = first + static_cast<int>(threadIdx.x); p <= last; p += kSkThreads)
-      part_slot[p - first] = 2 * p + (sk_unit_start(p, G, U) >= gu0 ? 0 : 1);
+      part_slot[p - first] = sku::part_slot(p, G, U, gu0);
     __syncthreads();
     // One float4 of the slot layout per thread and pass ([lane quarter][32-token
     // chunk][float4 i][lane]).  The sum is bound by L2 latency: every thread of the
