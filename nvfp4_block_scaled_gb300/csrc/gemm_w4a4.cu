@@ -620,9 +620,9 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 // columns for the scale slots), and D goes out with TMA stores.
 //
 // Tile schedules: static (pair p takes tiles p, p + P, ... of the grouped raster),
-// stream-K (pair_sched.h), or cluster launch control ([P1] Appendix): the grid holds
-// one cluster per tile, a running pair starts with its own tile and then cancels
-// pending clusters and takes theirs.  Warp 13 (otherwise idle) of the leader issues
+// stream-K (pair_sched.h), or cluster launch control (Colfax Research's SM120 NVFP4
+// GEMM article, Appendix): the grid holds one cluster per tile, a running pair starts
+// with its own tile and then cancels pending clusters and takes theirs.  Warp 13 (otherwise idle) of the leader issues
 // clusterlaunchcontrol.try_cancel with the response multicast to both CTAs into a
 // two-slot ring once every consuming role (27 warps or threads over the pair) has
 // read the slot's previous response; the follower's warp 13 arms its own barrier for

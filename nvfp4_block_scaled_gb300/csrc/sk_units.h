@@ -2,7 +2,7 @@
 // that compiles for the device and for the host (a host-side test checks the
 // invariants the kernel's tickets and fix-up rely on).
 //
-// [P2] Design, the persistent stream-K kernel: U units (token tile, 128-row group,
+// TileLang PR #3290, Design, the persistent stream-K kernel: U units (token tile, 128-row group,
 // 64-K step), group-major, split into G contiguous ranges, one per block.  A block's
 // range meets at most two groups only partly (the first and the last it touches);
 // every group it covers in between goes to the output whole.  The part of a split

@@ -1226,7 +1226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ tensor-core stream-K
 //
-// More than 32 tokens with a caller workspace ([P2] Design: the persistent stream-K
+// More than 32 tokens with a caller workspace (TileLang PR #3290, Design: the persistent stream-K
 // kernel over contiguous (tile, k-tile) ranges).  The units are (token tile, 128-row
 // group, 64-K step), group-major; block b of G takes units [b U / G, (b+1) U / G).  A
 // block walks its range as segments, one per (token tile, group) it touches: the same

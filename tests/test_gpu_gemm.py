@@ -402,7 +402,8 @@ def _config_index(tag):
 
 def test_clc_schedule_matches_static_pairs():
     # 12 x 12 = 144 tiles of 256 x 256 for ~76 co-resident CTA pairs: the first clusters
-    # cancel pending ones and take their tiles ([P1] Appendix, cluster launch control).
+    # cancel pending ones and take their tiles (Colfax Research's SM120 NVFP4 GEMM
+    # article, Appendix: cluster launch control).
     # Each tile is computed the same way under either schedule: identical bits.
     M = N = 3072
     K = 512

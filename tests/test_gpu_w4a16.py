@@ -210,7 +210,7 @@ def test_linear_colscale_rejects_bad_scale_pointer():
 
 
 def test_linear_more_than_1024_tokens():
-    # [P2] runs M > 1024 as 1024-row chunks; here token tiles of at most 256 cover
+    # TileLang PR #3290 runs M > 1024 as 1024-row chunks; here token tiles of at most 256 cover
     # any M in one launch.
     M, N, K = 1300, 256, 512
     x = G.bf16_normal(M, K, 8, "x")

@@ -1,6 +1,6 @@
 """The W4A16 tensor-core stream-K kernel's unit ranges (csrc/sk_units.h), compiled for
 the host and checked over many (token tiles, groups, K-steps, blocks) shapes, for the
-invariants its tickets and fix-up rely on ([P2] Design: contiguous (tile, k-tile)
+invariants its tickets and fix-up rely on (TileLang PR #3290, Design: contiguous (tile, k-tile)
 ranges, a deterministic fix-up):
 
 - the G ranges partition the U units, and cta_of finds the block of every unit;
